@@ -1,0 +1,227 @@
+/*
+ * pa.h — C ABI of libpa, the hot path of a paged-KV-cache attention engine
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Source pages (cited by title and section throughout this library):
+ *   [vLLM-wiki] itwiki.kr, "vLLM"
+ *   [MRV2]      llm-wiki.hwlabs.dev, "vLLM 0.25 Model Runner V2: 비동기 추론 경로의
+ *               재설계와 마이그레이션"
+ *   [V1-blog]   techknowgenie.com, "vLLM V1 코어 리팩토링 아키텍처: Zero-overhead C++
+ *               스케줄러와 Dynamic Chunked Prefill, PagedAttention v3 심층 분석"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Ownership: every buffer is allocated and owned by the caller. The library
+ *    never allocates, frees or keeps a pointer after the call returns, except
+ *    through work that it has enqueued on `stream`.
+ *  - Execution: every call enqueues kernels on `stream` (a cudaStream_t passed
+ *    as void*; NULL is the legacy default stream) and returns without waiting.
+ *    Only pa_get_error() synchronises.
+ *  - Host-side argument errors (NULL pointers, negative sizes, misaligned
+ *    pointers, inconsistent host mirrors) return PA_ERR_INVALID before any
+ *    launch; unsupported shapes return PA_ERR_UNSUPPORTED. A failed launch
+ *    returns PA_ERR_CUDA.
+ *  - Device-side range errors (a block id, slot or table row that points
+ *    outside its buffer) never fault: the kernel skips or clamps the offending
+ *    access and sets a sticky bit in a per-device error word, which
+ *    pa_get_error() reports and clears. Outputs of a call that raised a device
+ *    error are unspecified.
+ *  - All pointers marked "dev" are device pointers on the current device; "host"
+ *    pointers are read synchronously during the call only.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* pa_stream_t; /* a cudaStream_t */
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID = 1,       /* bad argument, detected on the host before launch   */
+  PA_ERR_UNSUPPORTED = 2,   /* shape or dtype outside the supported set           */
+  PA_ERR_CUDA = 3,          /* a CUDA runtime call failed                         */
+  PA_ERR_DEVICE_BOUNDS = 4, /* a kernel met an out-of-range index (pa_get_error)  */
+  PA_ERR_TIMEOUT = 5        /* a bounded device-side wait gave up (pa_get_error)  */
+} pa_status;
+
+typedef enum pa_kv_dtype {
+  PA_KV_BF16 = 0,     /* K/V stored as bfloat16                                  */
+  PA_KV_FP8_E4M3 = 1  /* K/V stored as OCP FP8 E4M3 codes with per-tensor scales */
+} pa_kv_dtype;
+
+/*
+ * The physical KV block pool.
+ * [vLLM-wiki, "블록 테이블"]: device memory is split ahead of time into equal-size
+ * physical blocks of `block_size` tokens; a request's logical blocks map to
+ * physical blocks that need not be contiguous.
+ *
+ * Layout (caller-owned device memory, 16-byte aligned), for K and V separately:
+ *     pool[num_blocks][num_kv_heads][block_size][head_dim]
+ * so the `block_size` tokens of one (block, kv-head) pair are one contiguous
+ * chunk of block_size*head_dim elements. Element type is bf16 (2 bytes) or an
+ * E4M3 code (1 byte) according to `dtype`.
+ *
+ * FP8 [vLLM-wiki, "엔진 구조와 주요 기능", quantisation bullet; V1-blog, "FP8 KV 캐시
+ * 양자화의 네이티브 통합"]: a stored code c represents decode(c) * k_scale (or
+ * v_scale). Scales are ignored for bf16 pools.
+ *
+ * Supported: head_dim in {64, 128}; block_size in {16, 32, 64}.
+ */
+typedef struct pa_kv_pool {
+  void* k_pool;          /* dev */
+  void* v_pool;          /* dev */
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t dtype;         /* pa_kv_dtype */
+  float k_scale;
+  float v_scale;
+} pa_kv_pool;
+
+/*
+ * pa_write_kv — scatter this step's new keys and values into the pool.
+ * [vLLM-wiki, "블록 테이블"] (slot = physical_block * block_size + offset) and
+ * [MRV2, "재설계 4"] (slot_mapping is prepared per token before the forward).
+ *
+ *   k_new, v_new   dev bf16 [T][num_kv_heads][head_dim], 16-byte aligned
+ *   slot_mapping   dev int64 [T]; slot < 0 marks a padding token (skipped)
+ *   T              number of tokens (0 is a no-op)
+ *
+ * For token t with s = slot_mapping[t] >= 0: blk = s / block_size,
+ * off = s % block_size, and for every kv head h and dim d
+ *     K[blk][h][off][d] = k_new[t][h][d]   (and the same for V).
+ * bf16 pools copy the bits. FP8 pools store e4m3(float(x) / scale), the
+ * quotient correctly rounded in fp32, then rounded to nearest-even with
+ * saturation to +-448; NaN stores 0x7F.
+ * A slot >= num_blocks*block_size sets PA_ERR_DEVICE_BOUNDS and is skipped.
+ * Duplicate slots within one call: which token wins is unspecified.
+ */
+pa_status pa_write_kv(const pa_kv_pool* pool, const void* k_new, const void* v_new,
+                      const int64_t* slot_mapping, int32_t T, pa_stream_t stream);
+
+/*
+ * pa_forward_workspace_size — bytes of optional scratch that lets pa_forward
+ * split long decode requests across CTAs (split-KV, merged by log-sum-exp).
+ * `max_splits` is the largest number of splits the caller wants per request.
+ * pa_forward works with any workspace size, including 0 (then each decode
+ * request is handled by one CTA per kv head).
+ */
+size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t head_dim,
+                                 int32_t max_splits);
+
+/*
+ * pa_forward — paged attention over a mixed batch of decode tokens and prefill
+ * chunks.
+ * [vLLM-wiki, "블록 단위 어텐션 계산", equation for A_ij and o_i]: the softmax runs
+ * across every visible key of every block of the request; the result equals
+ * ordinary attention, only the memory layout differs.
+ * [V1-blog, "고정 예산 기반 청크 분할 알고리즘"] and [vLLM-wiki, "엔진 구조와 주요 기능"
+ * unified-scheduler bullet]: one step packs one token per running decode next to
+ * prefill chunks.
+ * [MRV2, "재설계 4"]: query_start_loc and seq_lens describe the batch.
+ *
+ *   q                 dev bf16 [T][num_q_heads][head_dim], 16-byte aligned
+ *   out               dev bf16 [T][num_q_heads][head_dim], 16-byte aligned
+ *   query_start_loc   dev int32 [R+1], qsl[0]=0, non-decreasing, qsl[R]=T
+ *   seq_lens          dev int32 [R], all tokens of request r including this
+ *                     step's query tokens (whose K/V must already be written)
+ *   qsl_host, seq_lens_host
+ *                     host mirrors of the two arrays above (same values); used
+ *                     to plan grids without a device sync
+ *   block_tables      dev int32 [R][max_blocks]: physical block of logical
+ *                     block i of request r; entries past ceil(seq_len/B) unread
+ *   num_q_heads       Hq; must be a multiple of pool->num_kv_heads. Query head
+ *                     h reads kv head h / (Hq / Hkv) (contiguous GQA groups).
+ *   scale             softmax scale (e.g. 1/sqrt(head_dim))
+ *   causal            1: query j of request r (absolute position
+ *                     p = seq_len - q_len + j) sees keys 0..p. 0: every query
+ *                     sees keys 0..seq_len-1. A decode query (q_len == 1)
+ *                     sees all seq_len keys either way.
+ *   workspace         dev scratch of workspace_bytes (may be NULL/0)
+ *
+ * out[t][h][:] = sum_n softmax_n(scale * q[t][h] . k_n) v_n over the visible
+ * keys, computed in fp32 and rounded to bf16 (nearest-even). Rows of requests
+ * with q_len == 0 are not touched. Requests may appear in any order.
+ * Host checks: qsl_host must be non-decreasing with qsl_host[R] == T, and
+ * 1 <= q_len <= seq_len <= max_blocks * block_size for every request with
+ * q_len > 0; otherwise PA_ERR_INVALID.
+ */
+pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
+                     const int32_t* seq_lens, const int32_t* qsl_host,
+                     const int32_t* seq_lens_host, const int32_t* block_tables,
+                     int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                     int32_t num_q_heads, const pa_kv_pool* pool, float scale,
+                     int32_t causal, void* workspace, size_t workspace_bytes,
+                     pa_stream_t stream);
+
+/*
+ * pa_apply_staged_writes — apply packed block-table diffs, then gather the
+ * rows of this step.
+ * [MRV2, "재설계 3: 큰 block table은 staged diff만 보낸다"]: the device copy of the
+ * block table is the reference copy; the host records (row, start, values)
+ * diffs, uploads them in one small staging buffer, and one kernel applies them;
+ * the rows needed this step are then gathered by idx_mapping.
+ * [MRV2, "재설계 1"]: a request keeps a fixed persistent slot (row) while live;
+ * idx_mapping[i] is the slot of the i-th request of this batch.
+ * [MRV2, "재설계 2"]: the staging buffers must not be modified by the caller until
+ * the stream has consumed them.
+ *
+ *   table          dev int32 [max_reqs][max_blocks], updated in place
+ *   rows, starts   dev int32 [W]
+ *   val_offsets    dev int32 [W+1], non-decreasing; diff w writes
+ *                  len_w = val_offsets[w+1] - val_offsets[w] values
+ *   vals           dev int32 [val_offsets[W]]
+ *   idx_mapping    dev int32 [R]
+ *   gathered       dev int32 [R][max_blocks]
+ *
+ * For w = 0..W-1 in record order: table[rows[w]][starts[w] + k] =
+ * vals[val_offsets[w] + k], k < len_w (a later diff overwrites an earlier one
+ * on the same cell: last writer wins). Then gathered[i][c] =
+ * table[idx_mapping[i]][c] for every c < max_blocks. A diff whose row or
+ * column range leaves the table, or an idx_mapping entry outside
+ * [0, max_reqs), sets PA_ERR_DEVICE_BOUNDS and is skipped (gathered row left
+ * untouched). W == 0 performs only the gather; R == 0 only the writes.
+ */
+pa_status pa_apply_staged_writes(int32_t* table, int32_t max_reqs, int32_t max_blocks,
+                                 const int32_t* rows, const int32_t* starts,
+                                 const int32_t* val_offsets, const int32_t* vals,
+                                 int32_t W, const int32_t* idx_mapping, int32_t R,
+                                 int32_t* gathered, pa_stream_t stream);
+
+/*
+ * pa_copy_blocks — copy whole physical blocks (K and V, every kv head), the
+ * device half of copy-on-write.
+ * [vLLM-wiki, "블록 공유와 쓰기 시 복사"]: a block shared by several sequences is
+ * copied only when one of them must write a new token into it.
+ *
+ *   src, dst   dev int32 [n]; block src[i] is copied to block dst[i]
+ * The dst blocks must be distinct from each other and from every src block
+ * (then the copies are order-independent). An id outside [0, num_blocks) sets
+ * PA_ERR_DEVICE_BOUNDS and that pair is skipped.
+ */
+pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32_t* dst,
+                         int32_t n, pa_stream_t stream);
+
+/*
+ * pa_get_error — synchronise `stream`, then return and clear the sticky
+ * device error word of the current device: PA_ERR_TIMEOUT if a bounded wait
+ * gave up, else PA_ERR_DEVICE_BOUNDS if an index was out of range, else
+ * PA_OK. Returns PA_ERR_CUDA if the synchronisation itself failed.
+ */
+pa_status pa_get_error(pa_stream_t stream);
+
+/* pa_status_string — a static, human-readable name for a status code. */
+const char* pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */
