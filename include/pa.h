@@ -175,8 +175,9 @@ pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
  *
  *   table          dev int32 [max_reqs][max_blocks], updated in place
  *   rows, starts   dev int32 [W]
- *   val_offsets    dev int32 [W+1], non-decreasing; diff w writes
- *                  len_w = val_offsets[w+1] - val_offsets[w] values
+ *   val_offsets    dev int32 [W+1], non-decreasing from val_offsets[0] >= 0;
+ *                  diff w writes len_w = val_offsets[w+1] - val_offsets[w]
+ *                  values
  *   vals           dev int32 [val_offsets[W]]
  *   idx_mapping    dev int32 [R]
  *   gathered       dev int32 [R][max_blocks]
@@ -185,7 +186,8 @@ pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
  * vals[val_offsets[w] + k], k < len_w (a later diff overwrites an earlier one
  * on the same cell: last writer wins). Then gathered[i][c] =
  * table[idx_mapping[i]][c] for every c < max_blocks. A diff whose row or
- * column range leaves the table, or an idx_mapping entry outside
+ * column range leaves the table, whose value run leaves [0, val_offsets[W]),
+ * or an idx_mapping entry outside
  * [0, max_reqs), sets PA_ERR_DEVICE_BOUNDS and is skipped (gathered row left
  * untouched). W == 0 performs only the gather; R == 0 only the writes.
  */

@@ -185,7 +185,8 @@ int oracle_apply_staged_writes(int32_t* table, int32_t max_reqs, int32_t max_blo
     int32_t row = rows[w], start = starts[w];
     int32_t len = val_offsets[w + 1] - val_offsets[w];
     if (row < 0 || row >= max_reqs || start < 0 || len < 0 ||
-        (int64_t)start + len > max_blocks) {
+        (int64_t)start + len > max_blocks || val_offsets[w] < 0 ||
+        val_offsets[w + 1] > val_offsets[W]) {
       status = ORACLE_ERR_RANGE;
       continue;
     }

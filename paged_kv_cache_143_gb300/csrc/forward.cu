@@ -1,0 +1,132 @@
+// forward.cu — pa_forward: checks, planning from the host mirrors, dispatch of
+// the decode (split-KV + merge) and prefill kernels on the caller's stream.
+//
+// [vLLM-wiki "엔진 구조와 주요 기능"] (one token budget per step shared by decodes
+// and prefill chunks) and [V1-blog "고정 예산 기반 청크 분할 알고리즘"]: a step packs
+// one token per running decode next to prefill chunks; requests with q_len = 1
+// go to the decode kernels, requests with q_len > 1 to the prefill kernel.
+// [MRV2 "재설계 4"]: query_start_loc and seq_lens describe the batch; their host
+// mirrors let the planner size grids without a device synchronisation.
+#include <cmath>
+
+#include "pa_internal.h"
+#include "pa_kernels.h"
+
+namespace {
+
+size_t split_row_bytes(int64_t R, int64_t Hq, int64_t D) {
+  return (size_t)(R * Hq) * (size_t)(D * 4 + 8);
+}
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+extern "C" size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_heads,
+                                            int32_t head_dim, int32_t max_splits) {
+  if (num_reqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_splits <= 0) return 0;
+  return split_row_bytes(num_reqs, num_q_heads, head_dim) * (size_t)max_splits;
+}
+
+extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, const int32_t* qsl_host,
+                                const int32_t* seq_lens_host, const int32_t* block_tables,
+                                int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                                int32_t num_q_heads, const pa_kv_pool* pool, float scale,
+                                int32_t causal, void* workspace, size_t workspace_bytes,
+                                pa_stream_t stream) {
+  pa_status st = pa::check_pool(pool);
+  if (st != PA_OK) return st;
+  const int R = num_reqs, T = num_tokens, Hq = num_q_heads;
+  const int Hkv = pool->num_kv_heads, D = pool->head_dim, B = pool->block_size;
+  if (R < 0 || T < 0 || Hq <= 0 || max_blocks < 0) return PA_ERR_INVALID;
+  if (Hq % Hkv != 0) return PA_ERR_UNSUPPORTED;
+  const int g = Hq / Hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return PA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_INVALID;
+  if (causal != 0 && causal != 1) return PA_ERR_INVALID;
+  if (R == 0) return T == 0 ? PA_OK : PA_ERR_INVALID;
+  if (!qsl_host || !seq_lens_host || !query_start_loc || !seq_lens || !block_tables)
+    return PA_ERR_INVALID;
+  if (T > 0 && (!q || !out || !pa::aligned16(q) || !pa::aligned16(out))) return PA_ERR_INVALID;
+  if (workspace_bytes > 0 && (!workspace || !pa::aligned16(workspace))) return PA_ERR_INVALID;
+
+  // ---- plan from the host mirrors
+  if (qsl_host[0] != 0 || qsl_host[R] != T) return PA_ERR_INVALID;
+  int n_dec = 0, n_pre = 0, max_dec_seq = 0;
+  int64_t dec_keys = 0;
+  for (int r = 0; r < R; ++r) {
+    const int ql = qsl_host[r + 1] - qsl_host[r];
+    if (ql < 0) return PA_ERR_INVALID;
+    if (ql == 0) continue;
+    const int seq = seq_lens_host[r];
+    if (seq < ql || (int64_t)seq > (int64_t)max_blocks * B) return PA_ERR_INVALID;
+    if (ql == 1) {
+      ++n_dec;
+      dec_keys += seq;
+      if (seq > max_dec_seq) max_dec_seq = seq;
+    } else {
+      ++n_pre;
+    }
+  }
+  if (n_pre > 0) return PA_ERR_UNSUPPORTED;  // prefill kernel not built yet
+  unsigned* err = pa::error_word();
+  if (!err) return PA_ERR_CUDA;
+  cudaStream_t s = pa::as_stream(stream);
+  const bool fp8 = pool->dtype == PA_KV_FP8_E4M3;
+  const float kLog2e = 1.4426950408889634f;
+
+  if (n_dec > 0) {
+    pa::DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.qsl = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = g;
+    p.k_pool = static_cast<const uint8_t*>(pool->k_pool);
+    p.v_pool = static_cast<const uint8_t*>(pool->v_pool);
+    p.num_blocks = pool->num_blocks;
+    p.B = B;
+    p.q_scale = scale * kLog2e * (fp8 ? pool->k_scale : 1.f);
+    p.v_scale = fp8 ? pool->v_scale : 1.f;
+    p.err = err;
+
+    // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
+    // least 256 keys, a multiple of the 16-key chunk; bounded by the splits
+    // the workspace can hold. Depends only on seq_lens, never on placement.
+    const int gh = pa::decode_heads_per_cta(g);
+    const int64_t head_groups = (int64_t)Hkv * (g / gh);
+    const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
+    int64_t split = (dec_keys * head_groups + target_ctas - 1) / target_ctas;
+    if (split < 256) split = 256;
+    if (split > max_dec_seq) split = max_dec_seq;
+    split = round_up((int)split, 16);
+    const size_t row_bytes = split_row_bytes(R, Hq, D);
+    const int64_t ws_splits = row_bytes ? (int64_t)(workspace_bytes / row_bytes) : 0;
+    int max_splits = (int)((max_dec_seq + split - 1) / split);
+    if (max_splits > 1 && max_splits > ws_splits) {
+      if (ws_splits <= 1) {
+        split = round_up(max_dec_seq, 16);
+      } else {
+        split = round_up((int)((max_dec_seq + ws_splits - 1) / ws_splits), 16);
+      }
+      max_splits = (int)((max_dec_seq + split - 1) / split);
+    }
+    if (max_splits > 65535) return PA_ERR_UNSUPPORTED;
+    p.split_tokens = (int)split;
+    p.ws_splits = max_splits > 1 ? (int)ws_splits : 1;
+    if (max_splits > 1) {
+      p.ws_o = static_cast<float*>(workspace);
+      p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
+                                          (size_t)R * Hq * ws_splits * D * 4);
+    }
+    if (R > 65535) return PA_ERR_UNSUPPORTED;
+    if (pa::launch_decode(p, D, fp8, R, max_splits, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (max_splits > 1 && pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}

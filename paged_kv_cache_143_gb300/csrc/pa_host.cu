@@ -1,0 +1,87 @@
+// pa_host.cu — per-device error word, status strings, shared host checks.
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace {
+__device__ unsigned g_error_word;  // sticky bits: pa::kErrBounds | pa::kErrTimeout
+
+constexpr int kMaxDevices = 64;
+unsigned* g_word_addr[kMaxDevices];
+int g_sms[kMaxDevices];
+std::mutex g_mu;
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+namespace pa {
+
+unsigned* error_word() {
+  int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_word_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_word_addr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_word_addr[dev];
+}
+
+int num_sms() {
+  int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+pa_status check_pool(const pa_kv_pool* pool) {
+  if (!pool || !pool->k_pool || !pool->v_pool) return PA_ERR_INVALID;
+  if (!aligned16(pool->k_pool) || !aligned16(pool->v_pool)) return PA_ERR_INVALID;
+  if (pool->num_blocks < 0 || pool->num_kv_heads <= 0) return PA_ERR_INVALID;
+  if (pool->head_dim != 64 && pool->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (pool->block_size != 16 && pool->block_size != 32 && pool->block_size != 64)
+    return PA_ERR_UNSUPPORTED;
+  if (pool->dtype != PA_KV_BF16 && pool->dtype != PA_KV_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (pool->dtype == PA_KV_FP8_E4M3 &&
+      !(pool->k_scale > 0.0f && pool->v_scale > 0.0f && pool->k_scale < 3.0e38f &&
+        pool->v_scale < 3.0e38f))
+    return PA_ERR_INVALID;
+  return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_get_error(pa_stream_t stream) {
+  if (cudaStreamSynchronize(pa::as_stream(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned* w = pa::error_word();
+  if (!w) return PA_ERR_CUDA;
+  unsigned bits = 0;
+  if (cudaMemcpy(&bits, w, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (bits && cudaMemset(w, 0, sizeof bits) != cudaSuccess) return PA_ERR_CUDA;
+  if (bits & 2u) return PA_ERR_TIMEOUT;
+  if (bits & 1u) return PA_ERR_DEVICE_BOUNDS;
+  return PA_OK;
+}
+
+extern "C" const char* pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID: return "PA_ERR_INVALID: invalid argument";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA: CUDA runtime error";
+    case PA_ERR_DEVICE_BOUNDS: return "PA_ERR_DEVICE_BOUNDS: device index out of range";
+    case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: device wait gave up";
+  }
+  return "unknown pa_status";
+}

@@ -1,0 +1,30 @@
+// pa_internal.h — host-side helpers shared by the libpa translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Device address of the sticky error word of the current device (set up once
+// per device); nullptr if the runtime call failed.
+unsigned* error_word();
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+inline cudaStream_t as_stream(pa_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Maps the result of a launch (cudaGetLastError after <<<>>>) to a status.
+inline pa_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Shape checks shared by every entry point that takes a pool.
+pa_status check_pool(const pa_kv_pool* pool);
+
+}  // namespace pa

@@ -1,0 +1,190 @@
+"""Thin ctypes binding of libpa (C ABI in include/pa.h).
+
+Argument marshalling only: torch tensors are passed as raw device pointers,
+the stream as ``torch.cuda.current_stream().cuda_stream`` unless given, and
+every status other than PA_OK raises ``PaError``. All computation happens in
+the library's CUDA kernels; there is no fallback of any kind. The library is
+loaded from this package directory on first use (built with nvcc if it is
+absent) and a failure to load it raises immediately.
+"""
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_DEVICE_BOUNDS, PA_ERR_TIMEOUT = \
+    range(6)
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+
+# every function declared in include/pa.h
+EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
+           "pa_copy_blocks", "pa_get_error", "pa_status_string")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libpa (ctypes.CDLL). Raises if it cannot be built or loaded."""
+    global _lib
+    if _lib is None:
+        from . import build as _build
+        if not _build.up_to_date():
+            _build.build()
+        L = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F32, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                ctypes.c_size_t)
+        PP = ctypes.POINTER(_Pool)
+        L.pa_write_kv.restype = ctypes.c_int
+        L.pa_write_kv.argtypes = [PP, P, P, P, I32, P]
+        L.pa_forward_workspace_size.restype = SZ
+        L.pa_forward_workspace_size.argtypes = [I32, I32, I32, I32]
+        L.pa_forward.restype = ctypes.c_int
+        L.pa_forward.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32, I32, P, SZ, P]
+        L.pa_apply_staged_writes.restype = ctypes.c_int
+        L.pa_apply_staged_writes.argtypes = [P, I32, I32, P, P, P, P, I32, P, I32, P, P]
+        L.pa_copy_blocks.restype = ctypes.c_int
+        L.pa_copy_blocks.argtypes = [PP, P, P, I32, P]
+        L.pa_get_error.restype = ctypes.c_int
+        L.pa_get_error.argtypes = [P]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PaError(status, what)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dptr(t: Optional[torch.Tensor], dtype=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr() if t.numel() else None
+
+
+def _host_i32(a) -> np.ndarray:
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+class KVPool:
+    """Caller-owned K and V pools, each [num_blocks][Hkv][B][D] (bf16 or uint8
+    E4M3 codes), with per-tensor scales for FP8."""
+
+    def __init__(self, k: torch.Tensor, v: torch.Tensor, k_scale: float = 1.0,
+                 v_scale: float = 1.0):
+        if k.shape != v.shape or k.dim() != 4 or k.dtype != v.dtype:
+            raise ValueError("k and v pools must be [num_blocks][Hkv][B][D] of one dtype")
+        if k.dtype == torch.bfloat16:
+            self.dtype = PA_KV_BF16
+        elif k.dtype == torch.uint8:
+            self.dtype = PA_KV_FP8_E4M3
+        else:
+            raise TypeError("pool dtype must be bfloat16 or uint8 (E4M3 codes)")
+        self.k, self.v = k, v
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k.shape
+        self.k_scale, self.v_scale = float(k_scale), float(v_scale)
+
+    def struct(self) -> _Pool:
+        return _Pool(_dptr(self.k), _dptr(self.v), self.num_blocks, self.block_size,
+                     self.num_kv_heads, self.head_dim, self.dtype, self.k_scale, self.v_scale)
+
+
+def write_kv(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor,
+             slot_mapping: torch.Tensor, stream=None) -> None:
+    T = slot_mapping.numel()
+    st = lib().pa_write_kv(ctypes.byref(pool.struct()), _dptr(k_new, torch.bfloat16),
+                           _dptr(v_new, torch.bfloat16), _dptr(slot_mapping, torch.int64), T,
+                           _stream(stream))
+    _check(st, "pa_write_kv")
+
+
+def forward_workspace_size(num_reqs: int, num_q_heads: int, head_dim: int,
+                           max_splits: int) -> int:
+    return int(lib().pa_forward_workspace_size(num_reqs, num_q_heads, head_dim, max_splits))
+
+
+def forward(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
+            seq_lens: torch.Tensor, qsl_host, seq_lens_host, block_tables: torch.Tensor,
+            pool: KVPool, scale: float, causal: int = 1,
+            workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    qh = _host_i32(qsl_host)
+    sh = _host_i32(seq_lens_host)
+    R = sh.size
+    if qh.size != R + 1:
+        raise ValueError("qsl_host must have num_reqs + 1 entries")
+    T, Hq, D = q.shape
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    ws_ptr = _dptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pa_forward(
+        _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
+        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
+        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), ws_ptr, ws_bytes,
+        _stream(stream))
+    _check(st, "pa_forward")
+
+
+def apply_staged_writes(table: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,
+                        val_offsets: torch.Tensor, vals: torch.Tensor,
+                        idx_mapping: torch.Tensor, gathered: torch.Tensor, stream=None) -> None:
+    max_reqs, max_blocks = table.shape
+    W = rows.numel()
+    R = idx_mapping.numel()
+    st = lib().pa_apply_staged_writes(
+        _dptr(table, torch.int32), max_reqs, max_blocks, _dptr(rows, torch.int32),
+        _dptr(starts, torch.int32), _dptr(val_offsets, torch.int32), _dptr(vals, torch.int32),
+        W, _dptr(idx_mapping, torch.int32), R, _dptr(gathered, torch.int32), _stream(stream))
+    _check(st, "pa_apply_staged_writes")
+
+
+def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    st = lib().pa_copy_blocks(ctypes.byref(pool.struct()), _dptr(src, torch.int32),
+                              _dptr(dst, torch.int32), src.numel(), _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def get_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return int(lib().pa_get_error(_stream(stream)))

@@ -1,0 +1,52 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function
+that include/pa.h declares (no compute calls: runs without a GPU)."""
+import ctypes
+import os
+import re
+
+from paged_kv_cache_143_gb300 import pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(pa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(pa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(pa.lib()._name)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_host_side_rejections():
+    L = pa.lib()
+    assert pa.status_string(pa.PA_OK) == "PA_OK"
+    for s in range(6):
+        assert pa.status_string(s)
+    # argument errors are found on the host before any CUDA call
+    assert L.pa_write_kv(None, None, None, None, 1, None) == pa.PA_ERR_INVALID
+    assert L.pa_copy_blocks(None, None, None, 1, None) == pa.PA_ERR_INVALID
+    assert L.pa_apply_staged_writes(None, 1, 1, None, None, None, None, -1, None, 0, None,
+                                    None) == pa.PA_ERR_INVALID
+    pool = pa._Pool(16, 16, 4, 16, 1, 64, 0, 1.0, 1.0)
+    assert L.pa_write_kv(ctypes.byref(pool), None, None, None, 0, None) == pa.PA_OK
+    bad = pa._Pool(16, 16, 4, 24, 1, 64, 0, 1.0, 1.0)  # block size 24
+    assert L.pa_write_kv(ctypes.byref(bad), None, None, None, 0, None) == pa.PA_ERR_UNSUPPORTED
+    bad = pa._Pool(16, 16, 4, 16, 1, 96, 0, 1.0, 1.0)  # head dim 96
+    assert L.pa_copy_blocks(ctypes.byref(bad), None, None, 0, None) == pa.PA_ERR_UNSUPPORTED
+    fp8 = pa._Pool(16, 16, 4, 16, 1, 64, 1, 0.0, 1.0)  # FP8 with zero scale
+    assert L.pa_write_kv(ctypes.byref(fp8), None, None, None, 0, None) == pa.PA_ERR_INVALID
+    mis = pa._Pool(17, 16, 4, 16, 1, 64, 0, 1.0, 1.0)  # misaligned pool
+    assert L.pa_write_kv(ctypes.byref(mis), None, None, None, 0, None) == pa.PA_ERR_INVALID
+
+
+def test_workspace_size_formula():
+    assert pa.forward_workspace_size(256, 32, 128, 4) == 256 * 32 * 4 * (128 * 4 + 8)
+    assert pa.forward_workspace_size(0, 32, 128, 4) == 0
