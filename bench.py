@@ -1,0 +1,417 @@
+"""Benchmark of the paged-KV hot path on GB300.
+
+One step = one pass of the whole path over one batch: staged block-table diffs
++ gather (pa_apply_staged_writes), KV write of the step's tokens
+(pa_write_kv), attention (pa_forward). Workload: the 256-request decode batch
+of a 7B-like layer (32/32 heads, D 128, B 16, contexts U[128, 2048]); the
+metric is KV bytes the step's attention must read per second (GB/s), whole
+job over all GPUs (replicas: every rank runs its own batch).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libpa|reference]
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn decode KV GB/s vs HBM peak; mixed-batch tokens/s (1×GB300)"
+UNIT = "GB/s"
+CONFIG_ID = 2
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def traffic_for(kernel: str, src_files):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)[kernel]
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for p in src_files:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return t["bytes_per_launch"] if t.get("src_sha256") == h.hexdigest() else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4)
+                          if r[i].lower() in ("active", "0x1") or r[i] == "1"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+class Step:
+    """Device buffers of one step and the three C-ABI calls of the hot path."""
+
+    def __init__(self, w, dev, max_splits=32):
+        import torch
+        from paged_kv_cache_143_gb300 import pa
+        from workloads.generate import NAN_BF16, NAN_E4M3
+        self.w, self.pa = w, pa
+        shape = w.pool_shape()
+        if w.kv_dtype == "bf16":
+            k = torch.full(shape, NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+            v = torch.full(shape, NAN_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+        else:
+            k = torch.full(shape, NAN_E4M3, dtype=torch.uint8, device=dev)
+            v = torch.full(shape, NAN_E4M3, dtype=torch.uint8, device=dev)
+        self.pool = pa.KVPool(k, v, w.k_scale, w.v_scale)
+        if w.ctx_slots.numel():  # the cache before the step
+            pa.write_kv(self.pool, w.ctx_k, w.ctx_v, w.ctx_slots.to(dev))
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+        self.table = i32(w.table_before)
+        self.rows, self.starts = i32(w.diff_rows), i32(w.diff_starts)
+        self.offs, self.vals = i32(w.diff_val_offsets), i32(w.diff_vals)
+        self.idx = i32(w.idx_mapping)
+        self.gathered = torch.empty((w.R, w.max_blocks), dtype=torch.int32, device=dev)
+        self.qsl, self.seq = i32(w.qsl), i32(w.seq_lens)
+        self.q = w.q.to(dev).contiguous()
+        self.new_k, self.new_v = w.new_k.to(dev).contiguous(), w.new_v.to(dev).contiguous()
+        self.slots = w.slot_mapping.to(dev)
+        self.out = torch.empty_like(self.q)
+        n = pa.forward_workspace_size(w.R, w.Hq, w.D, max_splits)
+        self.ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+
+    def run(self):
+        pa, w = self.pa, self.w
+        pa.apply_staged_writes(self.table, self.rows, self.starts, self.offs, self.vals,
+                               self.idx, self.gathered)
+        pa.write_kv(self.pool, self.new_k, self.new_v, self.slots)
+        pa.forward(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens, self.gathered,
+                   self.pool, w.scale, w.causal, workspace=self.ws)
+
+
+def run_libpa(args):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    from paged_kv_cache_143_gb300 import accounting, pa
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = workloads.make(CONFIG_ID, device=dev, sub=rank, num_requests=args.requests)
+    kv_bytes = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+
+    step = Step(w, dev, max_splits=32)
+    stream = torch.cuda.current_stream()
+
+    # count this library's kernel launches in one step with the CUDA profiler
+    launches_per_step = None
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        step.run()
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step.run()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+        launches_per_step = sum(1 for n in names if any(
+            k in n for k in ("decode_kernel", "merge_kernel", "write_kv_kernel",
+                             "staged_writes_kernel", "prefill")))
+    except Exception:
+        launches_per_step = None
+
+    for _ in range(args.warmup):
+        step.run()
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        pa.apply_staged_writes(step.table, step.rows, step.starts, step.offs, step.vals,
+                               step.idx, step.gathered)
+        pa.write_kv(step.pool, step.new_k, step.new_v, step.slots)
+        ev[i][0].record(stream)
+        pa.forward(step.q, step.out, step.qsl, step.seq, w.qsl, w.seq_lens, step.gathered,
+                   step.pool, w.scale, w.causal, workspace=step.ws)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the timed region")
+    ms = t0.elapsed_time(t1) / args.steps
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([ms, fwd_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, fwd_ms = float(t[0]), float(t[1])
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside
+    e2e = run_e2e(args, w, step, dev, kv_bytes, world)
+
+    peak, peak_kind = load_peaks()
+    achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(kv_bytes * world / (ms * 1e-3) / 1e9, 2),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode-7b-like: {w.R} requests x 1 token, 32/32 heads, "
+                               f"head_dim 128, block 16, contexts U[128,2048] "
+                               f"({int(w.seq_lens.sum())} keys), bf16 KV",
+                   "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (KV read per step >> 129 MB)",
+                   "step": "pa_apply_staged_writes + pa_write_kv + pa_forward"},
+        "gpu_launches": (launches_per_step * args.steps) if launches_per_step else None,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"hbm_gbs ({peak_kind})",
+                     "kernel": "decode split-KV (pa_forward on a decode-only batch)",
+                     "ms_per_launch": round(fwd_ms, 5),
+                     "traffic": traffic_for("decode_kernel", [
+                         "paged_kv_cache_143_gb300/csrc/decode.cu",
+                         "paged_kv_cache_143_gb300/csrc/pa_device.cuh"])},
+        "e2e": e2e,
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, step, dev, kv_bytes, world):
+    """Same metric with the step's inputs copied from pinned host memory and the
+    output read back, inside the timed region, through the public C ABI."""
+    import torch
+    from paged_kv_cache_143_gb300 import pa
+
+    def pinned(t):
+        return t.detach().cpu().contiguous().pin_memory()
+    host_in = {
+        "q": pinned(w.q), "new_k": pinned(w.new_k), "new_v": pinned(w.new_v),
+        "slots": pinned(w.slot_mapping),
+        "rows": pinned(torch.from_numpy(w.diff_rows)),
+        "starts": pinned(torch.from_numpy(w.diff_starts)),
+        "offs": pinned(torch.from_numpy(w.diff_val_offsets)),
+        "vals": pinned(torch.from_numpy(w.diff_vals if w.diff_vals.size else
+                                        np.zeros(1, np.int32))),
+        "idx": pinned(torch.from_numpy(w.idx_mapping)),
+        "qsl": pinned(torch.from_numpy(w.qsl)), "seq": pinned(torch.from_numpy(w.seq_lens)),
+    }
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        d = dev_in
+        pa.apply_staged_writes(step.table, d["rows"][:w.diff_rows.size],
+                               d["starts"][:w.diff_starts.size], d["offs"], d["vals"],
+                               d["idx"], step.gathered)
+        pa.write_kv(step.pool, d["new_k"], d["new_v"], d["slots"])
+        pa.forward(d["q"], step.out, d["qsl"], d["seq"], w.qsl, w.seq_lens, step.gathered,
+                   step.pool, w.scale, w.causal, workspace=step.ws)
+        out_host.copy_(step.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    return {"value": round(kv_bytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------- oracle arms
+
+SAMPLE_REQUESTS = 64
+BASELINE_SECONDS = 10.0
+
+
+def oracle_sample_step(w):
+    """One step of the oracle on a sample workload: staged diffs + gather, KV
+    write, attention. Returns seconds."""
+    from oracle import oracle as O
+    from tests.helpers import bits, oracle_pool
+    pool = oracle_pool(w, include_new=False)
+    k_new, v_new, slots, q = bits(w.new_k), bits(w.new_v), w.slot_mapping.numpy(), bits(w.q)
+    t = time.perf_counter()
+    table = w.table_before.copy()
+    gathered = O.apply_staged_writes(table, w.diff_rows, w.diff_starts, w.diff_val_offsets,
+                                     w.diff_vals, w.idx_mapping)
+    O.write_kv(pool, k_new, v_new, slots)
+    O.paged_attention(q, w.qsl, w.seq_lens, gathered, pool, w.scale, w.causal)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(args, n_req=SAMPLE_REQUESTS):
+    import workloads
+    from oracle import oracle as O
+    from paged_kv_cache_143_gb300 import accounting
+    w = workloads.make(CONFIG_ID, device="cpu", sub=9, num_requests=n_req)
+    kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    secs = []
+    while not secs or sum(secs) < BASELINE_SECONDS:
+        secs.append(oracle_sample_step(w))
+    s = sum(secs) / len(secs)
+    return {"value": round(kv / s / 1e9, 4), "unit": UNIT, "cores": O.max_threads(),
+            "kind": "oracle", "seconds_per_step": round(s, 4), "steps": len(secs),
+            "sample": f"{len(secs)} steps of a {n_req}-request batch of the same decode "
+                      f"workload ({int(w.seq_lens.sum())} keys, {kv} KV bytes per step), "
+                      f"fp64 C oracle"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import workloads
+    from oracle import oracle as O
+    from paged_kv_cache_143_gb300 import accounting
+    n_req = SAMPLE_REQUESTS
+    w = workloads.make(CONFIG_ID, device="cpu", sub=9, num_requests=n_req)
+    kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    for _ in range(args.warmup):
+        oracle_sample_step(w)
+    secs = [oracle_sample_step(w) for _ in range(args.steps)]
+    s = sum(secs) / len(secs)
+    value = round(kv / s / 1e9, 4)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"decode-7b-like sample: {n_req} requests x 1 token, 32/32 heads, "
+                               f"head_dim 128, block 16, contexts U[128,2048]",
+                   "kv_bytes_per_step": kv},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n_req}-request sample of the decode workload per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["libpa", "reference"], default="libpa")
+    ap.add_argument("--requests", type=int, default=256,
+                    help="decode batch size (256 is the benchmark workload; smaller sizes "
+                         "are for profiling captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_libpa(args)
+
+
+if __name__ == "__main__":
+    main()
