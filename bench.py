@@ -173,22 +173,6 @@ def run_libpa(args):
     step = Step(w, dev, max_splits=32)
     stream = torch.cuda.current_stream()
 
-    # count this library's kernel launches in one step with the CUDA profiler
-    launches_per_step = None
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        step.run()
-        torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            step.run()
-            torch.cuda.synchronize()
-        names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
-        launches_per_step = sum(1 for n in names if any(
-            k in n for k in ("decode_kernel", "merge_kernel", "write_kv_kernel",
-                             "staged_writes_kernel", "prefill")))
-    except Exception:
-        launches_per_step = None
-
     for _ in range(args.warmup):
         step.run()
     if pa.get_error() != pa.PA_OK:
@@ -210,6 +194,7 @@ def run_libpa(args):
     time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = pa.kernel_launches()
     t0.record(stream)
     for i in range(args.steps):
         pa.apply_staged_writes(step.table, step.rows, step.starts, step.offs, step.vals,
@@ -220,6 +205,7 @@ def run_libpa(args):
                    step.pool, w.scale, w.causal, workspace=step.ws)
         ev[i][1].record(stream)
     t1.record(stream)
+    launches = pa.kernel_launches() - launches0
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
@@ -249,7 +235,7 @@ def run_libpa(args):
                    "kv_bytes_per_step": kv_bytes, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (KV read per step >> 129 MB)",
                    "step": "pa_apply_staged_writes + pa_write_kv + pa_forward"},
-        "gpu_launches": (launches_per_step * args.steps) if launches_per_step else None,
+        "gpu_launches": launches,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"hbm_gbs ({peak_kind})",

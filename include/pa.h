@@ -222,6 +222,13 @@ pa_status pa_get_error(pa_stream_t stream);
 /* pa_status_string — a static, human-readable name for a status code. */
 const char* pa_status_string(pa_status status);
 
+/*
+ * pa_kernel_launches — number of CUDA kernels this library has launched in
+ * this process (all devices, all streams), for launch accounting in
+ * benchmarks and tests. Not part of the method on the pages; never fails.
+ */
+uint64_t pa_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

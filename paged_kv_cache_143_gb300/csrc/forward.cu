@@ -126,7 +126,11 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     }
     if (R > 65535) return PA_ERR_UNSUPPORTED;
     if (pa::launch_decode(p, D, fp8, R, max_splits, s) != cudaSuccess) return PA_ERR_CUDA;
-    if (max_splits > 1 && pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+    pa::count_launches(1);
+    if (max_splits > 1) {
+      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+    }
   }
   return PA_OK;
 }

@@ -1,4 +1,5 @@
 // pa_host.cu — per-device error word, status strings, shared host checks.
+#include <atomic>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -10,6 +11,7 @@ constexpr int kMaxDevices = 64;
 unsigned* g_word_addr[kMaxDevices];
 int g_sms[kMaxDevices];
 std::mutex g_mu;
+std::atomic<unsigned long long> g_launches{0};
 
 int current_device() {
   int dev = -1;
@@ -44,6 +46,8 @@ int num_sms() {
   }
   return g_sms[dev];
 }
+
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 pa_status check_pool(const pa_kv_pool* pool) {
   if (!pool || !pool->k_pool || !pool->v_pool) return PA_ERR_INVALID;
@@ -84,4 +88,8 @@ extern "C" const char* pa_status_string(pa_status status) {
     case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT: device wait gave up";
   }
   return "unknown pa_status";
+}
+
+extern "C" uint64_t pa_kernel_launches(void) {
+  return g_launches.load(std::memory_order_relaxed);
 }

@@ -19,9 +19,16 @@ inline cudaStream_t as_stream(pa_stream_t s) { return reinterpret_cast<cudaStrea
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Maps the result of a launch (cudaGetLastError after <<<>>>) to a status.
+// Counts `n` kernel launches made by the library (reported by
+// pa_kernel_launches).
+void count_launches(unsigned n);
+
+// Maps the result of a launch (cudaGetLastError after <<<>>>) to a status and
+// counts the launch when it succeeded.
 inline pa_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  return PA_OK;
 }
 
 // Shape checks shared by every entry point that takes a pool.

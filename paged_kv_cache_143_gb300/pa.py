@@ -23,7 +23,7 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
-           "pa_copy_blocks", "pa_get_error", "pa_status_string")
+           "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches")
 
 
 class PaError(RuntimeError):
@@ -68,6 +68,8 @@ def lib():
         L.pa_get_error.argtypes = [P]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_kernel_launches.restype = ctypes.c_uint64
+        L.pa_kernel_launches.argtypes = []
         _lib = L
     return _lib
 
@@ -188,3 +190,8 @@ def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor, stream=None)
 def get_error(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device error status."""
     return int(lib().pa_get_error(_stream(stream)))
+
+
+def kernel_launches() -> int:
+    """Kernels launched by libpa so far in this process."""
+    return int(lib().pa_kernel_launches())
