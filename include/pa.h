@@ -223,6 +223,42 @@ pa_status pa_get_error(pa_stream_t stream);
 const char* pa_status_string(pa_status status);
 
 /*
+ * pa_forward_noalloc — pa_forward for callers that cannot allocate device
+ * memory. The pages have no counterpart of this call.
+ *
+ * Some callers may not call cudaMalloc (or any allocator) where they run
+ * attention: a plugin inside a host runtime that has reserved the device
+ * memory through its own pool and gives plugins no allocator, or a serving
+ * loop that forbids allocation after start-up because cudaMalloc can
+ * synchronise the device. This call takes the same arguments as pa_forward
+ * except the workspace: its split-KV scratch comes from a fixed array that
+ * the library keeps in device memory, PA_NOALLOC_SCRATCH_BYTES on every GPU
+ * that loads the library, held until the process exits.
+ *
+ *   max_splits   as in pa_forward_workspace_size; the scratch it needs,
+ *                pa_forward_workspace_size(num_reqs, num_q_heads, head_dim,
+ *                max_splits), must not exceed PA_NOALLOC_SCRATCH_BYTES, else
+ *                the call returns PA_ERR_UNSUPPORTED before any launch.
+ *                0 uses no scratch (one split per decode request).
+ *
+ * The call allocates nothing and frees nothing. The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress) and caches it;
+ * make that first call before any stream capture. Every call shares the same
+ * array: calls that may run at the same time on the GPU (different streams,
+ * or several host threads) race on it and must be serialised by the caller.
+ * The array keeps the previous call's contents; nothing needs clearing,
+ * because every cell a call reads is written earlier in that call.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+pa_status pa_forward_noalloc(const void* q, void* out, const int32_t* query_start_loc,
+                             const int32_t* seq_lens, const int32_t* qsl_host,
+                             const int32_t* seq_lens_host, const int32_t* block_tables,
+                             int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                             int32_t num_q_heads, const pa_kv_pool* pool, float scale,
+                             int32_t causal, int32_t max_splits, pa_stream_t stream);
+
+/*
  * pa_kernel_launches — number of CUDA kernels this library has launched in
  * this process (all devices, all streams), for launch accounting in
  * benchmarks and tests. Not part of the method on the pages; never fails.

@@ -23,7 +23,8 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
-           "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches")
+           "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
+           "pa_forward_noalloc")
 
 
 class PaError(RuntimeError):
@@ -68,6 +69,9 @@ def lib():
         L.pa_get_error.argtypes = [P]
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_status_string.argtypes = [ctypes.c_int]
+        L.pa_forward_noalloc.restype = ctypes.c_int
+        L.pa_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32, I32,
+                                         I32, P]
         L.pa_kernel_launches.restype = ctypes.c_uint64
         L.pa_kernel_launches.argtypes = []
         _lib = L
@@ -166,6 +170,33 @@ def forward(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
         Hq, ctypes.byref(pool.struct()), float(scale), int(causal), ws_ptr, ws_bytes,
         _stream(stream))
     _check(st, "pa_forward")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # PA_NOALLOC_SCRATCH_BYTES in include/pa.h
+
+
+def forward_noalloc(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
+                    seq_lens: torch.Tensor, qsl_host, seq_lens_host,
+                    block_tables: torch.Tensor, pool: KVPool, scale: float, causal: int = 1,
+                    max_splits: int = 32, stream=None) -> None:
+    """pa_forward for callers that cannot allocate device memory: the split-KV
+    scratch comes from the library's own fixed device array (16 MiB per GPU),
+    so no workspace is passed. Calls that may overlap on the GPU share that
+    array and must be serialised by the caller."""
+    qh = _host_i32(qsl_host)
+    sh = _host_i32(seq_lens_host)
+    R = sh.size
+    if qh.size != R + 1:
+        raise ValueError("qsl_host must have num_reqs + 1 entries")
+    T, Hq, D = q.shape
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    st = lib().pa_forward_noalloc(
+        _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
+        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
+        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), int(max_splits),
+        _stream(stream))
+    _check(st, "pa_forward_noalloc")
 
 
 def apply_staged_writes(table: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,
