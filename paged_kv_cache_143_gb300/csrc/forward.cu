@@ -53,7 +53,7 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
 
   // ---- plan from the host mirrors
   if (qsl_host[0] != 0 || qsl_host[R] != T) return PA_ERR_INVALID;
-  int n_dec = 0, n_pre = 0, max_dec_seq = 0;
+  int n_dec = 0, n_pre = 0, max_dec_seq = 0, max_q_tiles = 0;
   int64_t dec_keys = 0;
   for (int r = 0; r < R; ++r) {
     const int ql = qsl_host[r + 1] - qsl_host[r];
@@ -67,9 +67,12 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
       if (seq > max_dec_seq) max_dec_seq = seq;
     } else {
       ++n_pre;
+      const int tiles = (ql + 128 / g - 1) / (128 / g);
+      if (tiles > max_q_tiles) max_q_tiles = tiles;
     }
   }
-  if (n_pre > 0) return PA_ERR_UNSUPPORTED;  // prefill kernel not built yet
+  if (n_pre > 0 && pool->dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;  // FP8 prefill: next
+  if (R > 65535) return PA_ERR_UNSUPPORTED;
   unsigned* err = pa::error_word();
   if (!err) return PA_ERR_CUDA;
   cudaStream_t s = pa::as_stream(stream);
@@ -124,13 +127,39 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
       p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
                                           (size_t)R * Hq * ws_splits * D * 4);
     }
-    if (R > 65535) return PA_ERR_UNSUPPORTED;
     if (pa::launch_decode(p, D, fp8, R, max_splits, s) != cudaSuccess) return PA_ERR_CUDA;
     pa::count_launches(1);
     if (max_splits > 1) {
       if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
       pa::count_launches(1);
     }
+  }
+
+  if (n_pre > 0) {
+    pa::PrefillLaunch L{};
+    L.p.out = static_cast<__nv_bfloat16*>(out);
+    L.p.qsl = query_start_loc;
+    L.p.seq_lens = seq_lens;
+    L.p.block_tables = block_tables;
+    L.p.max_blocks = max_blocks;
+    L.p.Hq = Hq;
+    L.p.Hkv = Hkv;
+    L.p.g = g;
+    L.p.num_blocks = pool->num_blocks;
+    L.p.B = B;
+    L.p.causal = causal;
+    L.p.scale_log2 = scale * kLog2e;
+    L.p.err = err;
+    L.q = q;
+    L.k_pool = pool->k_pool;
+    L.v_pool = pool->v_pool;
+    L.T = T;
+    L.R = R;
+    L.D = D;
+    L.max_q_tiles = max_q_tiles;
+    if (pool->num_blocks == 0) return PA_ERR_INVALID;
+    if (pa::launch_prefill(L, s) != cudaSuccess) return PA_ERR_CUDA;
+    pa::count_launches(1);
   }
   return PA_OK;
 }

@@ -31,6 +31,30 @@ struct DecodeParams {
 // Query heads handled by one decode CTA for GQA group size g.
 int decode_heads_per_cta(int g);
 
+struct PrefillParams {
+  __nv_bfloat16* out;          // [T][Hq][D]
+  const int32_t* qsl;          // [R+1]
+  const int32_t* seq_lens;     // [R]
+  const int32_t* block_tables; // [R][max_blocks]
+  int32_t max_blocks;
+  int32_t Hq, Hkv, g;
+  int32_t num_blocks, B;
+  int32_t causal;
+  float scale_log2;            // softmax scale * log2(e)
+  unsigned* err;
+};
+
+struct PrefillLaunch {
+  PrefillParams p;
+  const void* q;               // bf16 [T][Hq][D]
+  const void* k_pool;          // [num_blocks][Hkv][B][D]
+  const void* v_pool;
+  int32_t T, R, D;
+  int32_t max_q_tiles;         // max over prefill requests of ceil(q_len * g / 128)
+};
+
+cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s);
+
 cudaError_t launch_decode(const DecodeParams& p, int D, bool fp8, int R, int max_splits,
                           cudaStream_t s);
 cudaError_t launch_merge(const DecodeParams& p, int D, int R, cudaStream_t s);
