@@ -247,11 +247,94 @@ def run_libpa(args):
         "e2e": e2e,
         "clocks": clk,
     }
+    del step
+    torch.cuda.empty_cache()
+    line["mixed_batch"] = run_mixed(args, dev, 3)
+    line["long_context"] = {"bf16": run_mixed(args, dev, 5, "bf16")}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def timed(fn, steps, warmup, stream):
+    """Mean ms of fn() over `steps` calls after `warmup`, CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_mixed(args, dev, cfg, kv_dtype=None):
+    """Mixed decode + prefill step of config `cfg` (tokens/s of the whole step),
+    and the prefill kernel alone on the same chunks (causal TFLOP/s)."""
+    import torch
+    import workloads
+    from paged_kv_cache_143_gb300 import accounting, pa
+    stream = torch.cuda.current_stream()
+    w = workloads.make(cfg, device=dev, kv_dtype=kv_dtype)
+    step = Step(w, dev, max_splits=32)
+    ms = timed(step.run, args.steps, args.warmup, stream)
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the mixed step")
+    ql = np.diff(w.qsl)
+    chunks = np.nonzero(ql > 1)[0]
+    pairs = sum(accounting.causal_pairs(int(ql[r]), int(w.seq_lens[r])) for r in chunks)
+    flops = accounting.attention_flops(pairs, w.Hq, w.D)
+    dec = np.nonzero(ql == 1)[0]
+    dec_bytes = accounting.decode_kv_bytes(w.seq_lens[dec], w.Hkv, w.D, w.elt_bytes)
+    # the chunks alone: only the prefill kernel runs in pa_forward
+    wp = workloads.build(w.seq_lens[chunks], ql[chunks], w.Hq, w.Hkv, w.D, w.B,
+                         kv_dtype=w.kv_dtype, seed=workloads.config_seed(cfg, 1), device=dev)
+    sp = Step(wp, dev, max_splits=32)
+    sp.run()
+    fwd = lambda: pa.forward(sp.q, sp.out, sp.qsl, sp.seq, wp.qsl, wp.seq_lens, sp.gathered,
+                             sp.pool, wp.scale, wp.causal, workspace=sp.ws)
+    ms_pre = timed(fwd, args.steps, args.warmup, stream)
+    # the decodes alone
+    wd = workloads.build(w.seq_lens[dec], ql[dec], w.Hq, w.Hkv, w.D, w.B, kv_dtype=w.kv_dtype,
+                         seed=workloads.config_seed(cfg, 2), device=dev)
+    sd = Step(wd, dev, max_splits=32)
+    sd.run()
+    fwd_d = lambda: pa.forward(sd.q, sd.out, sd.qsl, sd.seq, wd.qsl, wd.seq_lens, sd.gathered,
+                               sd.pool, wd.scale, wd.causal, workspace=sd.ws)
+    ms_dec = timed(fwd_d, args.steps, args.warmup, stream)
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the split runs")
+    peak_t = load_peaks_tensor()
+    tf = flops / (ms_pre * 1e-3) / 1e12
+    del step, sp, sd
+    torch.cuda.empty_cache()
+    return {
+        "workload": w.name, "tokens_per_step": int(w.T), "ms_per_step": round(ms, 4),
+        "tokens_per_s": round(w.T / (ms * 1e-3), 1),
+        "step": "pa_apply_staged_writes + pa_write_kv + pa_forward (decodes and chunks)",
+        "prefill_only": {"ms": round(ms_pre, 4), "causal_flops": int(flops),
+                         "tflops": round(tf, 1),
+                         "roofline": {"bound": "tensor", "achieved": round(tf, 1),
+                                      "peak": peak_t, "unit": "TFLOP/s",
+                                      "frac": round(tf / peak_t, 4),
+                                      "peak_source": "bf16_tflops (measured, burst)"}},
+        "decode_only": {"ms": round(ms_dec, 4), "kv_bytes": int(dec_bytes),
+                        "gbs": round(dec_bytes / (ms_dec * 1e-3) / 1e9, 1)},
+    }
+
+
+def load_peaks_tensor():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
 
 
 def run_e2e(args, w, step, dev, kv_bytes, world):
