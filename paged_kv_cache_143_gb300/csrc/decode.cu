@@ -118,35 +118,50 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
-      const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
-      int issued = 0;
-      for (int c = 0; c < nch; ++c) {
-        const int stage = c % kStages, round = c / kStages;
-        if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
-          tail->abort = 1;
-          break;
+    // The warp fetches the block ids of 32 chunks at a time (lane i: chunk
+    // base + i, one coalesced load); lane 0 issues the bulk copies.
+    const unsigned full = 0xffffffffu;
+    const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
+    const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
+    int issued = 0;
+    bool ok = true;
+    for (int base = 0; base < nch && ok; base += 32) {
+      const int c_lane = base + lane;
+      const int key_lane = k_begin + c_lane * kChunk;
+      int blk_lane = c_lane < nch ? __ldg(table + key_lane / p.B) : 0;
+      const bool bad = c_lane < nch && (blk_lane < 0 || blk_lane >= p.num_blocks);
+      if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
+      if (bad) blk_lane = 0;  // read a valid block; the call's output is then unspecified
+      const int n = min(32, nch - base);
+      for (int i = 0; i < n; ++i) {
+        const int c = base + i;
+        const int blk = __shfl_sync(full, blk_lane, i);
+        if (lane == 0) {
+          const int stage = c % kStages, round = c / kStages;
+          if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
+            tail->abort = 1;
+            ok = false;
+          } else if (*reinterpret_cast<volatile int*>(&tail->abort)) {
+            ok = false;
+          } else {
+            const int key0 = k_begin + c * kChunk;
+            const int64_t off = ((int64_t)blk * p.Hkv + kvh) * head_stride +
+                                (int64_t)(key0 % p.B) * G::kRowBytes;
+            uint8_t* dst = ring + stage * G::kStageBytes;
+            mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
+            bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
+            bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
+            issued = c + 1;
+          }
         }
-        if (*reinterpret_cast<volatile int*>(&tail->abort)) break;
-        const int key0 = k_begin + c * kChunk;
-        int blk = table[key0 / p.B];
-        if (blk < 0 || blk >= p.num_blocks) {
-          raise_error(p.err, kErrBounds);
-          blk = 0;  // read a valid block; the call's output is then unspecified
-        }
-        const int64_t off = ((int64_t)blk * p.Hkv + kvh) * head_stride +
-                            (int64_t)(key0 % p.B) * G::kRowBytes;
-        uint8_t* dst = ring + stage * G::kStageBytes;
-        mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
-        bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
-        bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
-        issued = c + 1;
+        ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
       }
-      // drain: every issued copy has landed before the CTA may exit
+    }
+    // drain: every issued copy has landed before the CTA may exit
+    if (lane == 0)
       for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
         mbar_wait(&tail->full[c % kStages], (c / kStages) & 1, p.err);
-    }
     return;
   }
 

@@ -7,6 +7,7 @@
 // go to the decode kernels, requests with q_len > 1 to the prefill kernel.
 // [MRV2 "재설계 4"]: query_start_loc and seq_lens describe the batch; their host
 // mirrors let the planner size grids without a device synchronisation.
+#include <algorithm>
 #include <cmath>
 
 #include "pa_internal.h"
@@ -157,6 +158,21 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     L.R = R;
     L.D = D;
     L.max_q_tiles = max_q_tiles;
+    // launch the requests with the most causal (query, key) pairs first so
+    // that their long-running tiles do not form the tail of the grid
+    if (n_pre <= pa::kMaxOrderedPrefill) {
+      int n = 0;
+      for (int r = 0; r < R; ++r)
+        if (qsl_host[r + 1] - qsl_host[r] > 1) L.p.order[n++] = r;
+      auto work = [&](int r) {
+        const int64_t ql = qsl_host[r + 1] - qsl_host[r];
+        const int64_t P = seq_lens_host[r] - ql;
+        return causal ? ql * P + ql * (ql + 1) / 2 : ql * (int64_t)seq_lens_host[r];
+      };
+      std::stable_sort(L.p.order, L.p.order + n,
+                       [&](int a, int b) { return work(a) > work(b); });
+      L.p.n_order = n;
+    }
     if (pool->num_blocks == 0) return PA_ERR_INVALID;
     if (pa::launch_prefill(L, s) != cudaSuccess) return PA_ERR_CUDA;
     pa::count_launches(1);

@@ -31,6 +31,8 @@ struct DecodeParams {
 // Query heads handled by one decode CTA for GQA group size g.
 int decode_heads_per_cta(int g);
 
+constexpr int kMaxOrderedPrefill = 256;
+
 struct PrefillParams {
   __nv_bfloat16* out;          // [T][Hq][D]
   const int32_t* qsl;          // [R+1]
@@ -42,6 +44,10 @@ struct PrefillParams {
   int32_t causal;
   float scale_log2;            // softmax scale * log2(e)
   unsigned* err;
+  // prefill requests in launch order (most work first); n_order == 0 means
+  // grid.z walks every request in batch order
+  int32_t n_order;
+  int32_t order[kMaxOrderedPrefill];
 };
 
 struct PrefillLaunch {

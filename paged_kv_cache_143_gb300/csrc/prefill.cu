@@ -14,14 +14,15 @@
 //   warp 0     TMA producer: the Q tile once (a 4-D tensor map over
 //              [T][Hkv][g][D]), then per 128-key tile one 2-D box per physical
 //              block (coordinates from the block table) for K and for V,
-//              into a 2-stage ring, 128-byte swizzled;
+//              into a 3-stage ring, 128-byte swizzled (K of a stage is
+//              released after its S MMA, V after its PV MMA);
 //   warp 1     allocates 512 TMEM columns and issues the MMAs from one thread:
 //              S_j = Q K_j^T (M 128, N 128, K = D; both operands K-major) into
 //              one of two S buffers, and O += P_j V_j (M 128, N = D, K 128; P
-//              K-major, V MN-major) into the O accumulator;
+//              read from TMEM, V MN-major from shared memory) into O;
 //   warps 2-5  softmax, one TMEM lane (= one query row) per thread: read S,
-//              mask, online max/sum in log2 units, write P as bf16 into a
-//              double-buffered swizzled shared tile; O is rescaled in TMEM
+//              mask, online max/sum in log2 units, write P as bf16 pairs into
+//              one of two TMEM P buffers; O is rescaled in TMEM
 //              only when the running max grows by more than 2^8 (the stale
 //              max is otherwise kept, which is exact algebra); epilogue O/l.
 // Every wait is bounded; a timeout sets the error word and the CTA unwinds
@@ -40,7 +41,7 @@ namespace {
 
 constexpr int kM = 128;        // query rows per tile
 constexpr int kN = 128;        // keys per KV tile
-constexpr int kStages = 2;     // KV tiles in flight
+constexpr int kStages = 3;     // KV tiles in flight
 constexpr int kThreads = 192;  // 6 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -51,12 +52,10 @@ struct Smem {
   static constexpr int kChunks = D / 64;
   static constexpr int kQBytes = kM * D * 2;
   static constexpr int kKVBytes = kN * D * 2;
-  static constexpr int kPBytes = kM * kN * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kAlloc = kBytes + 1024;  // the base is rounded up to 1024 B
 };
@@ -65,7 +64,8 @@ struct Bars {
   uint64_t q_full;
   uint64_t k_full[kStages];
   uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_empty[kStages];  // K of a stage is free once its S MMA is done
+  uint64_t v_empty[kStages];  // V of a stage is free once its PV MMA is done
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + S::kOffBar);
 
-  const int r = blockIdx.z;
+  const int r = p.n_order ? p.order[blockIdx.z] : (int)blockIdx.z;
   const int q_begin = p.qsl[r];
   const int q_len = p.qsl[r + 1] - q_begin;
   if (q_len <= 1) return;  // decode requests and empty requests are not ours
@@ -122,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -142,9 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   const uint32_t tmem_o = tmem + 2 * kN;  // columns [256, 256 + D)
+  const uint32_t tmem_p = tmem + 3 * kN;  // P_b (bf16 pairs) at columns [384 + 64 b, +64)
 
   if (warp == 0) {
     // ----------------------------------------------------------- TMA producer
+    // The whole warp walks the tiles: lane i fetches the block id of entry i
+    // of the next tile (one coalesced load, in flight while this tile waits);
+    // lane 0 issues the copies with the ids broadcast by shuffle.
+    const unsigned full = 0xffffffffu;
     if (lane == 0) {
       tc::prefetch_tensormap(&tmap_q);
       tc::prefetch_tensormap(&tmap_k);
@@ -153,46 +159,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < S::kChunks; ++c)
         tc::tma_load_4d(smem + S::kOffQ + c * S::kChunkBytes, &tmap_q, c * 64, 0, kvh,
                         q_begin + q0, &bars->q_full);
-      const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
-      const int nbt = kN / p.B;  // blocks per KV tile
-      int issued = 0;
-      for (int j = 0; j < ntk; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages &&
-            !mbar_wait(&bars->kv_empty[st], ((j / kStages) - 1) & 1, p.err)) {
-          bars->abort = 1;
-          break;
-        }
-        if (aborted(bars)) break;
-        int nload = 0;
-        while (nload < nbt && (j * nbt + nload) * p.B < n_kv) ++nload;
-        const uint32_t bytes = (uint32_t)(nload * p.B * D * 2);
-        uint8_t* ks = smem + S::kOffK + st * S::kKVBytes;
-        uint8_t* vs = smem + S::kOffV + st * S::kKVBytes;
-        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-        for (int i = 0; i < nload; ++i) {
-          int blk = table[j * nbt + i];
-          if (blk < 0 || blk >= p.num_blocks) {
-            raise_error(p.err, kErrBounds);
-            blk = 0;
-          }
-          const int row = (blk * p.Hkv + kvh) * p.B;
-          for (int c = 0; c < S::kChunks; ++c)
-            tc::tma_load_2d(ks + c * S::kChunkBytes + i * p.B * 128, &tmap_k, c * 64, row,
-                            &bars->k_full[st]);
-        }
-        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-        for (int i = 0; i < nload; ++i) {
-          int blk = table[j * nbt + i];
-          if (blk < 0 || blk >= p.num_blocks) blk = 0;
-          const int row = (blk * p.Hkv + kvh) * p.B;
-          for (int c = 0; c < S::kChunks; ++c)
-            tc::tma_load_2d(vs + c * S::kChunkBytes + i * p.B * 128, &tmap_v, c * 64, row,
-                            &bars->v_full[st]);
-        }
-        issued = j + 1;
+    }
+    const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
+    const int nbt = kN / p.B;  // blocks per KV tile (<= 8)
+    auto fetch = [&](int j) -> int {
+      const int lb = j * nbt + lane;
+      return (j < ntk && lane < nbt && lb * p.B < n_kv) ? __ldg(table + lb) : 0;
+    };
+    int ids = fetch(0);
+    int issued = 0;
+    // lane -> one box of the tile: tensor (K, V), block i, 64-column chunk c
+    const int box_tensor = lane >> 4;
+    const int box_block = (lane & 15) / S::kChunks;
+    const int box_chunk = (lane & 15) % S::kChunks;
+    for (int j = 0; j < ntk; ++j) {
+      const int next = fetch(j + 1);
+      const int st = j % kStages;
+      bool ok = true;
+      if (lane == 0 && j >= kStages)
+        ok = mbar_wait(&bars->k_empty[st], ((j / kStages) - 1) & 1, p.err) &&
+             mbar_wait(&bars->v_empty[st], ((j / kStages) - 1) & 1, p.err);
+      ok = __shfl_sync(full, ok ? 1 : 0, 0) && !aborted(bars);
+      if (!ok) {
+        if (lane == 0) bars->abort = 1;
+        break;
       }
-      // every issued copy lands before the CTA may leave
+      int nload = 0;
+      while (nload < nbt && (j * nbt + nload) * p.B < n_kv) ++nload;
+      const bool bad = lane < nload && (ids < 0 || ids >= p.num_blocks);
+      if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
+      const int blk_lane = bad ? 0 : ids;  // a valid block; the output is then unspecified
+      const int blk = __shfl_sync(full, blk_lane, box_block & 7);
+      const uint32_t bytes = (uint32_t)(nload * p.B * D * 2);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+      }
+      __syncwarp();
+      if (box_block < nload) {
+        const int row = (blk * p.Hkv + kvh) * p.B;
+        uint8_t* dst = smem + (box_tensor ? S::kOffV : S::kOffK) + st * S::kKVBytes +
+                       box_chunk * S::kChunkBytes + box_block * p.B * 128;
+        tc::tma_load_2d(dst, box_tensor ? &tmap_v : &tmap_k, box_chunk * 64, row,
+                        box_tensor ? &bars->v_full[st] : &bars->k_full[st]);
+      }
+      issued = j + 1;
+      ids = next;
+    }
+    // every issued copy lands before the CTA may leave
+    if (lane == 0) {
       mbar_wait(&bars->q_full, 0, p.err);
       for (int j = issued - kStages > 0 ? issued - kStages : 0; j < issued; ++j) {
         mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err);
@@ -211,17 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&bars->v_full[st], (jj / kStages) & 1, p.err)) return false;
         if (aborted(bars)) return false;
         tc::fence_after_sync();
-        const uint8_t* ps = smem + S::kOffP + bb * S::kPBytes;
         const uint8_t* vs = smem + S::kOffV + st * S::kKVBytes;
 #pragma unroll
         for (int ks = 0; ks < kN / 16; ++ks) {
-          const uint64_t a = tc::smem_desc_sw128(ps + (ks >> 2) * S::kChunkBytes + (ks & 3) * 32,
-                                                 16, 1024);
           const uint64_t b = tc::smem_desc_sw128(vs + ks * 16 * 128, S::kChunkBytes, 1024);
-          tc::mma_bf16_ss(tmem_o, a, b, idesc_o, jj > 0 || ks > 0);
+          tc::mma_bf16_ts(tmem_o, tmem_p + bb * (kN / 2) + ks * 8, b, idesc_o, jj > 0 || ks > 0);
         }
         tc::mma_commit(&bars->pv_done[bb]);
-        tc::mma_commit(&bars->kv_empty[st]);
+        tc::mma_commit(&bars->v_empty[st]);
         return true;
       };
       bool ok = mbar_wait(&bars->q_full, 0, p.err);
@@ -242,6 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_bf16_ss(tmem + b * kN, a, bd, idesc_s, ks > 0);
         }
         tc::mma_commit(&bars->s_full[b]);
+        tc::mma_commit(&bars->k_empty[st]);
         if (j >= 1 && !issue_pv(j - 1)) ok = false;
       }
       if (ok) ok = issue_pv(ntk - 1);
@@ -269,14 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       float s[kN];
       {
-        uint32_t raw[32];
+        uint32_t raw[kN / 32][32];
 #pragma unroll
-        for (int c = 0; c < kN / 32; ++c) {
-          tc::tmem_ld32(tmem + b * kN + c * 32 + lane_off, raw);
-          tc::tmem_wait_ld();
+        for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(tmem + b * kN + c * 32 + lane_off, raw[c]);
+        tc::tmem_wait_ld();
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(raw[k]) * p.scale_log2;
-        }
+        for (int c = 0; c < kN / 32; ++c)
+#pragma unroll
+          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(raw[c][k]);
       }
       const int key0 = j * kN;
       if (key0 + kN > limit) {
@@ -284,9 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < kN; ++k)
           if (key0 + k >= limit) s[k] = -INFINITY;
       }
-      float mt = -INFINITY;
+      // raw scores; the log2-domain max is max * scale_log2 (scale > 0).
+      // Eight independent partial maxima keep the reduction off one long
+      // dependency chain (one softmax warp per SM sub-partition has no other
+      // warp to hide latency with).
+      float mx[8];
 #pragma unroll
-      for (int k = 0; k < kN; ++k) mt = fmaxf(mt, s[k]);
+      for (int u = 0; u < 8; ++u) mx[u] = s[u];
+#pragma unroll
+      for (int k = 8; k < kN; k += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], s[k + u]);
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      mt *= p.scale_log2;
       float m_use = m_run, alpha = 1.f;
       bool rescale = false;
       if (m_run == -INFINITY) {
@@ -298,12 +322,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      float rs = 0.f;
+      float sum[8];
 #pragma unroll
-      for (int k = 0; k < kN; ++k) {
-        s[k] = fast_exp2(s[k] - m_sub);
-        rs += s[k];
-      }
+      for (int u = 0; u < 8; ++u) sum[u] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kN; k += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          s[k + u] = fast_exp2(fmaf(s[k + u], p.scale_log2, -m_sub));
+          sum[u] += s[k + u];
+        }
+      const float rs = ((sum[0] + sum[1]) + (sum[2] + sum[3])) +
+                       ((sum[4] + sum[5]) + (sum[6] + sum[7]));
       l_run = l_run * alpha + rs;
       m_run = m_use;
 
@@ -313,24 +343,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      uint8_t* ps = smem + S::kOffP + b * S::kPBytes;
+      // P as bf16 pairs into this row's TMEM lane (the A operand of PV)
 #pragma unroll
-      for (int c = 0; c < kN / 64; ++c)
+      for (int c = 0; c < kN / 64; ++c) {
+        uint32_t w[32];
 #pragma unroll
-        for (int gq = 0; gq < 8; ++gq) {
-          const float* f = s + c * 64 + gq * 8;
-          uint4 v;
-          __nv_bfloat162 h0 = __floats2bfloat162_rn(f[0], f[1]);
-          __nv_bfloat162 h1 = __floats2bfloat162_rn(f[2], f[3]);
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(f[4], f[5]);
-          __nv_bfloat162 h3 = __floats2bfloat162_rn(f[6], f[7]);
-          v.x = *reinterpret_cast<uint32_t*>(&h0);
-          v.y = *reinterpret_cast<uint32_t*>(&h1);
-          v.z = *reinterpret_cast<uint32_t*>(&h2);
-          v.w = *reinterpret_cast<uint32_t*>(&h3);
-          *reinterpret_cast<uint4*>(ps + c * S::kChunkBytes + row * 128 +
-                                    ((gq ^ (row & 7)) << 4)) = v;
+        for (int k = 0; k < 32; ++k) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
+          w[k] = *reinterpret_cast<uint32_t*>(&h);
         }
+        tc::tmem_st32(tmem_p + b * (kN / 2) + c * 32 + lane_off, w);
+      }
+      tc::tmem_wait_st();
 
       // rescale O (rare): needs PV(j-1) complete
       if (__any_sync(0xffffffffu, rescale)) {
@@ -474,7 +498,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(L.max_q_tiles, p.Hkv, L.R);
+  dim3 grid(L.max_q_tiles, p.Hkv, p.n_order ? p.n_order : L.R);
   prefill_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
