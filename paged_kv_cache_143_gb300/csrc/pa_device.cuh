@@ -100,9 +100,12 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
-// Named barrier over `count` threads (a multiple of 32), id 1..15.
+// Named barrier over `count` threads (a multiple of 32). The caller's warp
+// is reconverged first, and the non-aligned form is used, so a warp whose
+// lanes arrive from different branches cannot leave the barrier incomplete.
 __device__ __forceinline__ void named_bar_sync(unsigned id, unsigned count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------------ numbers

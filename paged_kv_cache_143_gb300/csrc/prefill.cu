@@ -8,23 +8,27 @@
 // 알고리즘"]: a prefill chunk of q_len tokens follows P = seq_len - q_len cached
 // tokens, so query j of the chunk sits at absolute position P + j.
 //
-// One CTA = one tile of 128 query rows x one kv head. The rows are the
-// (token, head) pairs of the GQA group that shares the kv head, packed token
-// major (row = token * g + head), so K/V are read once per group.
-//   warp 0     TMA producer: the Q tile once (a 4-D tensor map over
-//              [T][Hkv][g][D]), then per 128-key tile one 2-D box per physical
-//              block (coordinates from the block table) for K and for V,
-//              into a 3-stage ring, 128-byte swizzled (K of a stage is
-//              released after its S MMA, V after its PV MMA);
-//   warp 1     allocates 512 TMEM columns and issues the MMAs from one thread:
-//              S_j = Q K_j^T (M 128, N 128, K = D; both operands K-major) into
-//              one of two S buffers, and O += P_j V_j (M 128, N = D, K 128; P
-//              read from TMEM, V MN-major from shared memory) into O;
-//   warps 2-5  softmax, one TMEM lane (= one query row) per thread: read S,
-//              mask, online max/sum in log2 units, write P as bf16 pairs into
-//              one of two TMEM P buffers; O is rescaled in TMEM
-//              only when the running max grows by more than 2^8 (the stale
-//              max is otherwise kept, which is exact algebra); epilogue O/l.
+// One CTA = two consecutive tiles (A, B) of 128 query rows x one kv head; both
+// tiles share every K/V tile that is loaded. A tile's rows are the (token,
+// head) pairs of the GQA group that shares the kv head, packed token major
+// (row = token * g + head), so K/V are read once per group.
+//   warpgroup 0  warp 0: TMA producer — the Q tiles once (a 4-D tensor map over
+//                [T][Hkv][g][D]), then per 128-key tile one 2-D box per physical
+//                block and 64-column chunk (coordinates from the block table),
+//                all boxes of a tile issued by one warp instruction, into a
+//                ring of stages (K of a stage released after its S MMAs, V
+//                after its PV MMAs);
+//                warp 1: allocates 512 TMEM columns; one thread issues the MMAs
+//                in the order PV_A(j-1), S_A(j), PV_B(j-1), S_B(j), so that one
+//                tile's MMAs run while the other tile's softmax works:
+//                S_t = Q_t K_j^T (M 128, N 128, K = D, both operands K-major,
+//                f32 in TMEM) and O_t += P_t V_j (P_t read from TMEM where it
+//                overwrote S_t, V MN-major from shared memory).
+//   warpgroups 1, 2  softmax of tiles A and B, one TMEM lane (= one query row)
+//                per thread: read S, mask, online max/sum in log2 units, write
+//                P as bf16 pairs over S; O is rescaled in TMEM only when the
+//                running max grows by more than 2^8 (the stale max is otherwise
+//                kept, which is exact algebra); epilogue O / l.
 // Every wait is bounded; a timeout sets the error word and the CTA unwinds
 // (waits for its copies and MMAs, frees TMEM) without writing output.
 #include <cudaTypedefs.h>
@@ -41,19 +45,30 @@ namespace {
 
 constexpr int kM = 128;        // query rows per tile
 constexpr int kN = 128;        // keys per KV tile
-constexpr int kStages = 3;     // KV tiles in flight
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
+// Register split: the block is launched with kLaunchRegs per thread (the
+// __launch_bounds__ cap for 384 threads); warpgroup 0 lowers to
+// kRegsProducer and the two softmax warpgroups raise to kRegsSoftmax. The
+// raised total must not exceed the launched total, or the raise never
+// completes.
+constexpr uint32_t kLaunchRegs = 168;
+constexpr uint32_t kRegsProducer = 64;
+constexpr uint32_t kRegsSoftmax = 216;
+static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * kLaunchRegs,
+              "register split exceeds the registers the block is launched with");
+static_assert(kRegsProducer % 8 == 0 && kRegsSoftmax % 8 == 0, "setmaxnreg takes multiples of 8");
 
 template <int D>
 struct Smem {
-  static constexpr int kChunkBytes = kN * 128;          // 128 rows x 64 bf16 (one swizzle column)
+  static constexpr int kStages = D == 128 ? 2 : 4;     // KV tiles in flight
+  static constexpr int kChunkBytes = kN * 128;         // 128 rows x 64 bf16 (one swizzle column)
   static constexpr int kChunks = D / 64;
-  static constexpr int kQBytes = kM * D * 2;
-  static constexpr int kKVBytes = kN * D * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kQBytes = kM * D * 2;           // one Q tile
+  static constexpr int kKVBytes = kN * D * 2;          // one K or V tile
+  static constexpr int kOffQ = 0;                      // Q_A, then Q_B
+  static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kStages * kKVBytes;
   static constexpr int kBytes = kOffBar + 256;
@@ -62,11 +77,11 @@ struct Smem {
 
 struct Bars {
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t k_empty[kStages];  // K of a stage is free once its S MMA is done
-  uint64_t v_empty[kStages];  // V of a stage is free once its PV MMA is done
-  uint64_t s_full[2];
+  uint64_t k_full[4];
+  uint64_t v_full[4];
+  uint64_t k_empty[4];  // K of a stage is free once its S MMAs are done
+  uint64_t v_empty[4];  // V of a stage is free once its PV MMAs are done
+  uint64_t s_full[2];   // per Q tile
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t final_mma;
@@ -90,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, PrefillParams p) {
   using S = Smem<D>;
+  constexpr int kStages = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -102,9 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g = p.g;
   const int tpt = kM / g;  // tokens per tile
   const int ntq = (q_len + tpt - 1) / tpt;
-  if ((int)blockIdx.x >= ntq) return;
-  const int tile = ntq - 1 - (int)blockIdx.x;  // heaviest (latest) tiles start first
-  const int q0 = tile * tpt;
+  const int npairs = (ntq + 1) / 2;
+  if ((int)blockIdx.x >= npairs) return;
+  const int pair = npairs - 1 - (int)blockIdx.x;  // heaviest (latest) pairs start first
   const int kvh = blockIdx.y;
   const int seq = p.seq_lens[r];
   if (seq < q_len || seq > p.max_blocks * p.B) {
@@ -112,9 +128,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int P = seq - q_len;
-  const int last_tok = min(q_len, q0 + tpt) - 1;
-  const int n_kv = p.causal ? min(seq, P + last_tok + 1) : seq;
-  const int ntk = (n_kv + kN - 1) / kN;
+  int q0[2], ntk[2], n_kv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int tile = 2 * pair + t;
+    q0[t] = tile * tpt;
+    if (tile < ntq) {
+      const int last = min(q_len, q0[t] + tpt) - 1;
+      n_kv[t] = p.causal ? min(seq, P + last + 1) : seq;
+      ntk[t] = (n_kv[t] + kN - 1) / kN;
+    } else {
+      n_kv[t] = 0;
+      ntk[t] = 0;
+    }
+  }
+  const int ntk_all = max(ntk[0], ntk[1]);
+  const int n_kv_all = max(n_kv[0], n_kv[1]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -125,10 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->p_full[b], 4);  // one arrival per softmax warp
-      mbar_init(&bars->pv_done[b], 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&bars->pv_done[t], 1);
     }
     mbar_init(&bars->final_mma, 1);
     bars->abort = 0;
@@ -141,166 +170,191 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  const uint32_t tmem = bars->tmem_base;
-  const uint32_t tmem_o = tmem + 2 * kN;  // columns [256, 256 + D)
-  const uint32_t tmem_p = tmem + 3 * kN;  // P_b (bf16 pairs) at columns [384 + 64 b, +64)
+  const uint32_t tmem = bars->tmem_base;  // S_t / P_t at column 128 t, O_t at 256 + 128 t
 
-  if (warp == 0) {
+  // Warpgroup 0 (producer, MMA, two idle warps) gives registers to the two
+  // softmax warpgroups (see kRegsProducer / kRegsSoftmax). The role branches never merge
+  // (each ends with its own block-wide barrier), so each keeps its limit.
+  if (warp < 4) {
+    tc::regs_dec<kRegsProducer>();
+    if (warp == 0) {
     // ----------------------------------------------------------- TMA producer
-    // The whole warp walks the tiles: lane i fetches the block id of entry i
-    // of the next tile (one coalesced load, in flight while this tile waits);
-    // lane 0 issues the copies with the ids broadcast by shuffle.
     const unsigned full = 0xffffffffu;
     if (lane == 0) {
       tc::prefetch_tensormap(&tmap_q);
       tc::prefetch_tensormap(&tmap_k);
       tc::prefetch_tensormap(&tmap_v);
-      mbar_arrive_expect_tx(&bars->q_full, S::kQBytes);
-      for (int c = 0; c < S::kChunks; ++c)
-        tc::tma_load_4d(smem + S::kOffQ + c * S::kChunkBytes, &tmap_q, c * 64, 0, kvh,
-                        q_begin + q0, &bars->q_full);
+      const int nq = ntk[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&bars->q_full, nq * S::kQBytes);
+      for (int t = 0; t < nq; ++t)
+        for (int c = 0; c < S::kChunks; ++c)
+          tc::tma_load_4d(smem + S::kOffQ + t * S::kQBytes + c * S::kChunkBytes, &tmap_q,
+                          c * 64, 0, kvh, q_begin + q0[t], &bars->q_full);
     }
     const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
     const int nbt = kN / p.B;  // blocks per KV tile (<= 8)
     auto fetch = [&](int j) -> int {
       const int lb = j * nbt + lane;
-      return (j < ntk && lane < nbt && lb * p.B < n_kv) ? __ldg(table + lb) : 0;
+      return (j < ntk_all && lane < nbt && lb * p.B < n_kv_all) ? __ldg(table + lb) : 0;
     };
+    // lane -> one box of a K or V tile: block i, 64-column chunk c
+    const int box_block = lane / S::kChunks;
+    const int box_chunk = lane % S::kChunks;
     int ids = fetch(0);
-    int issued = 0;
-    // lane -> one box of the tile: tensor (K, V), block i, 64-column chunk c
-    const int box_tensor = lane >> 4;
-    const int box_block = (lane & 15) / S::kChunks;
-    const int box_chunk = (lane & 15) % S::kChunks;
-    for (int j = 0; j < ntk; ++j) {
+    int issued_k = 0, issued_v = 0;
+    for (int j = 0; j < ntk_all; ++j) {
       const int next = fetch(j + 1);
       const int st = j % kStages;
-      bool ok = true;
-      if (lane == 0 && j >= kStages)
-        ok = mbar_wait(&bars->k_empty[st], ((j / kStages) - 1) & 1, p.err) &&
-             mbar_wait(&bars->v_empty[st], ((j / kStages) - 1) & 1, p.err);
-      ok = __shfl_sync(full, ok ? 1 : 0, 0) && !aborted(bars);
-      if (!ok) {
-        if (lane == 0) bars->abort = 1;
-        break;
-      }
       int nload = 0;
-      while (nload < nbt && (j * nbt + nload) * p.B < n_kv) ++nload;
+      while (nload < nbt && (j * nbt + nload) * p.B < n_kv_all) ++nload;
       const bool bad = lane < nload && (ids < 0 || ids >= p.num_blocks);
       if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
       const int blk_lane = bad ? 0 : ids;  // a valid block; the output is then unspecified
       const int blk = __shfl_sync(full, blk_lane, box_block & 7);
       const uint32_t bytes = (uint32_t)(nload * p.B * D * 2);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-        mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+      const bool issues = box_block < nload;
+      const int row = (blk * p.Hkv + kvh) * p.B;
+      const int dst_off = st * S::kKVBytes + box_chunk * S::kChunkBytes + box_block * p.B * 128;
+      // K of tile j: its stage is free once the S MMAs of tile j - kStages are done
+      bool ok = true;
+      if (lane == 0 && j >= kStages)
+        ok = mbar_wait(&bars->k_empty[st], ((j / kStages) - 1) & 1, p.err);
+      if (!__shfl_sync(full, ok ? 1 : 0, 0) || aborted(bars)) {
+        if (lane == 0) bars->abort = 1;
+        break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
       __syncwarp();
-      if (box_block < nload) {
-        const int row = (blk * p.Hkv + kvh) * p.B;
-        uint8_t* dst = smem + (box_tensor ? S::kOffV : S::kOffK) + st * S::kKVBytes +
-                       box_chunk * S::kChunkBytes + box_block * p.B * 128;
-        tc::tma_load_2d(dst, box_tensor ? &tmap_v : &tmap_k, box_chunk * 64, row,
-                        box_tensor ? &bars->v_full[st] : &bars->k_full[st]);
+      if (issues)
+        tc::tma_load_2d(smem + S::kOffK + dst_off, &tmap_k, box_chunk * 64, row, &bars->k_full[st]);
+      issued_k = j + 1;
+      // V of tile j: free once the PV MMAs of tile j - kStages are done
+      if (lane == 0 && j >= kStages)
+        ok = mbar_wait(&bars->v_empty[st], ((j / kStages) - 1) & 1, p.err);
+      if (!__shfl_sync(full, ok ? 1 : 0, 0)) {
+        if (lane == 0) bars->abort = 1;
+        break;
       }
-      issued = j + 1;
+      if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+      __syncwarp();
+      if (issues)
+        tc::tma_load_2d(smem + S::kOffV + dst_off, &tmap_v, box_chunk * 64, row, &bars->v_full[st]);
+      issued_v = j + 1;
       ids = next;
     }
     // every issued copy lands before the CTA may leave
     if (lane == 0) {
       mbar_wait(&bars->q_full, 0, p.err);
-      for (int j = issued - kStages > 0 ? issued - kStages : 0; j < issued; ++j) {
+      for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
         mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err);
+      for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
         mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err);
-      }
     }
-  } else if (warp == 1) {
+    } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kM, kN, false, false);
       constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kM, D, false, true);
-      const uint8_t* qs = smem + S::kOffQ;
-      auto issue_pv = [&](int jj) -> bool {
-        const int bb = jj & 1, st = jj % kStages;
-        if (!mbar_wait(&bars->p_full[bb], (jj >> 1) & 1, p.err)) return false;
-        if (!mbar_wait(&bars->v_full[st], (jj / kStages) & 1, p.err)) return false;
+      bool ok = mbar_wait(&bars->q_full, 0, p.err);
+      auto issue_s = [&](int t, int j) {
+        const uint8_t* qs = smem + S::kOffQ + t * S::kQBytes;
+        const uint8_t* ks = smem + S::kOffK + (j % kStages) * S::kKVBytes;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t a =
+              tc::smem_desc_sw128(qs + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
+          const uint64_t b =
+              tc::smem_desc_sw128(ks + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
+          tc::mma_bf16_ss(tmem + t * kN, a, b, idesc_s, k > 0);
+        }
+        tc::mma_commit(&bars->s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!mbar_wait(&bars->p_full[t], j & 1, p.err)) return false;
+        if (!mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err)) return false;
         if (aborted(bars)) return false;
         tc::fence_after_sync();
-        const uint8_t* vs = smem + S::kOffV + st * S::kKVBytes;
+        const uint8_t* vs = smem + S::kOffV + (j % kStages) * S::kKVBytes;
 #pragma unroll
-        for (int ks = 0; ks < kN / 16; ++ks) {
-          const uint64_t b = tc::smem_desc_sw128(vs + ks * 16 * 128, S::kChunkBytes, 1024);
-          tc::mma_bf16_ts(tmem_o, tmem_p + bb * (kN / 2) + ks * 8, b, idesc_o, jj > 0 || ks > 0);
+        for (int k = 0; k < kN / 16; ++k) {
+          const uint64_t b = tc::smem_desc_sw128(vs + k * 16 * 128, S::kChunkBytes, 1024);
+          tc::mma_bf16_ts(tmem + 2 * kN + t * kN, tmem + t * kN + k * 8, b, idesc_o,
+                          j > 0 || k > 0);
         }
-        tc::mma_commit(&bars->pv_done[bb]);
-        tc::mma_commit(&bars->v_empty[st]);
+        tc::mma_commit(&bars->pv_done[t]);
         return true;
       };
-      bool ok = mbar_wait(&bars->q_full, 0, p.err);
-      for (int j = 0; ok && j < ntk; ++j) {
-        const int st = j % kStages, b = j & 1;
+      for (int j = 0; ok && j < ntk_all; ++j) {
+        const int st = j % kStages;
         if (!mbar_wait(&bars->k_full[st], (j / kStages) & 1, p.err) || aborted(bars)) {
           ok = false;
           break;
         }
         tc::fence_after_sync();
-        const uint8_t* ks_ = smem + S::kOffK + st * S::kKVBytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t a =
-              tc::smem_desc_sw128(qs + (ks >> 2) * S::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              tc::smem_desc_sw128(ks_ + (ks >> 2) * S::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + b * kN, a, bd, idesc_s, ks > 0);
+        for (int t = 0; t < 2; ++t) {
+          // PV_t(j-1) reads P_t out of the S_t columns before S_t(j) overwrites them
+          if (j >= 1 && j - 1 < ntk[t] && !issue_pv(t, j - 1)) ok = false;
+          if (ok && j < ntk[t]) issue_s(t, j);
         }
-        tc::mma_commit(&bars->s_full[b]);
         tc::mma_commit(&bars->k_empty[st]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        if (j >= 1) tc::mma_commit(&bars->v_empty[(j - 1) % kStages]);
       }
-      if (ok) ok = issue_pv(ntk - 1);
+      if (ok) {
+        const int j = ntk_all - 1;
+        for (int t = 0; t < 2 && ok; ++t)
+          if (j < ntk[t] && !issue_pv(t, j)) ok = false;
+        tc::mma_commit(&bars->v_empty[j % kStages]);
+      }
       if (!ok) bars->abort = 1;
       tc::mma_commit(&bars->final_mma);
       mbar_wait(&bars->final_mma, 0, p.err);
     }
+    }
+    // teardown: after every thread of the block is done with TMEM
+    tc::fence_before_sync();
+    named_bar_sync(0, kThreads);
+    if (warp == 1) {
+      tc::fence_after_sync();
+      tc::tmem_dealloc(tmem, kTmemCols);
+    }
   } else {
-    // -------------------------------------------------------------- softmax
+    tc::regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax
+    const int t = warp >= 8 ? 1 : 0;  // Q tile of this warpgroup
+    const int my_ntk = t ? ntk[1] : ntk[0];
+    const int my_q0 = t ? q0[1] : q0[0];
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int tok = q0 + row / g;
+    const uint32_t tmem_s = tmem + t * kN + lane_off;
+    const uint32_t tmem_o = tmem + 2 * kN + t * kN + lane_off;
+    const int tok = my_q0 + row / g;
     const int head = row % g;
-    const bool valid_row = tok < q_len;
+    const bool valid_row = my_ntk > 0 && tok < q_len;
     const int limit = !valid_row ? 0 : (p.causal ? min(P + tok + 1, seq) : seq);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < ntk; ++j) {
-      const int b = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[b], (j >> 1) & 1, p.err))) {
+    for (int j = 0; j < my_ntk; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, p.err))) {
         ok = false;
         break;
       }
       tc::fence_after_sync();
-      float s[kN];
-      {
-        uint32_t raw[kN / 32][32];
+      uint32_t sr[kN];
 #pragma unroll
-        for (int c = 0; c < kN / 32; ++c) tc::tmem_ld32(tmem + b * kN + c * 32 + lane_off, raw[c]);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < kN / 32; ++c)
-#pragma unroll
-          for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(raw[c][k]);
-      }
+      for (int c = 0; c < kN / 32; ++c)
+        tc::tmem_ld32(tmem_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+      tc::tmem_wait_ld();
+      float* s = reinterpret_cast<float*>(sr);
       const int key0 = j * kN;
       if (key0 + kN > limit) {
 #pragma unroll
         for (int k = 0; k < kN; ++k)
           if (key0 + k >= limit) s[k] = -INFINITY;
       }
-      // raw scores; the log2-domain max is max * scale_log2 (scale > 0).
-      // Eight independent partial maxima keep the reduction off one long
-      // dependency chain (one softmax warp per SM sub-partition has no other
-      // warp to hide latency with).
+      // raw scores; the log2-domain max is max * scale_log2 (scale > 0);
+      // eight independent partial maxima keep the reduction off one chain
       float mx[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mx[u] = s[u];
@@ -332,34 +386,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[k + u] = fast_exp2(fmaf(s[k + u], p.scale_log2, -m_sub));
           sum[u] += s[k + u];
         }
-      const float rs = ((sum[0] + sum[1]) + (sum[2] + sum[3])) +
-                       ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-      l_run = l_run * alpha + rs;
+      l_run = l_run * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
+                               ((sum[4] + sum[5]) + (sum[6] + sum[7])));
       m_run = m_use;
 
-      // the P buffer b is free once PV(j-2) has finished
-      if (j >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[b], ((j - 2) >> 1) & 1, p.err))) {
-        ok = false;
-        break;
-      }
-      // P as bf16 pairs into this row's TMEM lane (the A operand of PV)
-#pragma unroll
-      for (int c = 0; c < kN / 64; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
-          w[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        tc::tmem_st32(tmem_p + b * (kN / 2) + c * 32 + lane_off, w);
-      }
-      tc::tmem_wait_st();
-
-      // rescale O (rare): needs PV(j-1) complete
+      // rescale O_t (rare): PV_t(j-1) precedes S_t(j) in the MMA stream, so it
+      // has completed; the wait only orders the TMEM accesses
       if (__any_sync(0xffffffffu, rescale)) {
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[t], (j - 1) & 1, p.err))) {
           ok = false;
           break;
         }
@@ -368,24 +402,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
-          tc::tmem_ld32(tmem_o + c * 32 + lane_off, o);
+          tc::tmem_ld32(tmem_o + c * 32, o);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
-          tc::tmem_st32(tmem_o + c * 32 + lane_off, o);
+          tc::tmem_st32(tmem_o + c * 32, o);
         }
-        tc::tmem_wait_st();
       }
-
-      // the last tile may hold keys past n_kv (unloaded blocks, unwritten
-      // cells): zero those V rows so that P = 0 never meets a NaN
-      if (j == ntk - 1 && key0 + kN > n_kv) {
+      // P as bf16 pairs over the first 64 columns of S_t (the A operand of PV)
+#pragma unroll
+      for (int c = 0; c < kN / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
+          w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        tc::tmem_st32(tmem_s + c * 32, w);
+      }
+      tc::tmem_wait_st();
+      // the CTA's last tile may hold keys past n_kv_all (unloaded blocks,
+      // unwritten cells): zero those V rows so that P = 0 never meets a NaN
+      if (j == ntk_all - 1 && key0 + kN > n_kv_all) {
         const int st = j % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j / kStages) & 1, p.err))) {
           ok = false;
           break;
         }
-        if (key0 + row >= n_kv) {
+        if (key0 + row >= n_kv_all) {
           uint8_t* vs = smem + S::kOffV + st * S::kKVBytes;
 #pragma unroll
           for (int c = 0; c < S::kChunks; ++c)
@@ -394,27 +438,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(vs + c * S::kChunkBytes + row * 128 + q * 16) =
                   make_uint4(0, 0, 0, 0);
         }
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full[b]);
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
 
-    // epilogue: O / l once the last PV has landed
-    if (ok && !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[(ntk - 1) & 1],
-                                                 ((ntk - 1) >> 1) & 1, p.err)))
+    // epilogue: O_t / l once its last PV has landed
+    if (ok && my_ntk > 0 &&
+        !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[t], (my_ntk - 1) & 1, p.err)))
       ok = false;
     if (!ok) bars->abort = 1;
-    if (ok && !aborted(bars)) {
+    if (ok && my_ntk > 0 && !aborted(bars)) {
       tc::fence_after_sync();
       const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow =
-          p.out + ((int64_t)(q_begin + tok) * p.Hq + kvh * g + head) * D;
+      __nv_bfloat16* orow = p.out + ((int64_t)(q_begin + tok) * p.Hq + kvh * g + head) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tc::tmem_ld32(tmem_o + c * 32 + lane_off, o);
+        tc::tmem_ld32(tmem_o + c * 32, o);
         tc::tmem_wait_ld();
         if (valid_row) {
 #pragma unroll
@@ -432,13 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  }
-
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 1) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    tc::fence_before_sync();
+    named_bar_sync(0, kThreads);
   }
 }
 
@@ -498,7 +536,13 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(L.max_q_tiles, p.Hkv, p.n_order ? p.n_order : L.R);
+  // the register split inside the kernel assumes the block is launched with
+  // kLaunchRegs per thread; refuse to launch a build that allocated fewer
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+  if (e != cudaSuccess) return e;
+  if (fa.numRegs < (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
+  dim3 grid((L.max_q_tiles + 1) / 2, p.Hkv, p.n_order ? p.n_order : L.R);  // tile pairs
   prefill_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

@@ -43,6 +43,20 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ----------------------------------------------------- register rebalancing
+
+// Lowers / raises the per-thread register limit of the executing warpgroup
+// (all four warps must execute the same instruction). The sum over the
+// block's warpgroups must stay within the registers it was launched with.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
 // ------------------------------------------------------------------- TMEM
 
 // Allocates `ncols` (power of two >= 32) TMEM columns; the whole warp must
