@@ -72,7 +72,6 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
       if (tiles > max_q_tiles) max_q_tiles = tiles;
     }
   }
-  if (n_pre > 0 && pool->dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;  // FP8 prefill: next
   if (R > 65535) return PA_ERR_UNSUPPORTED;
   unsigned* err = pa::error_word();
   if (!err) return PA_ERR_CUDA;
@@ -149,7 +148,9 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     L.p.num_blocks = pool->num_blocks;
     L.p.B = B;
     L.p.causal = causal;
-    L.p.scale_log2 = scale * kLog2e;
+    L.p.scale_log2 = scale * kLog2e * (fp8 ? pool->k_scale : 1.f);
+    L.p.v_scale = fp8 ? pool->v_scale : 1.f;
+    L.fp8 = fp8;
     L.p.err = err;
     L.q = q;
     L.k_pool = pool->k_pool;

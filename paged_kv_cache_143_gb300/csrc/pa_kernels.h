@@ -42,7 +42,8 @@ struct PrefillParams {
   int32_t Hq, Hkv, g;
   int32_t num_blocks, B;
   int32_t causal;
-  float scale_log2;            // softmax scale * log2(e)
+  float scale_log2;            // softmax scale * log2(e) (* k_scale for E4M3 pools)
+  float v_scale;               // v_scale for E4M3 pools, else 1
   unsigned* err;
   // prefill requests in launch order (most work first); n_order == 0 means
   // grid.z walks every request in batch order
@@ -56,6 +57,7 @@ struct PrefillLaunch {
   const void* k_pool;          // [num_blocks][Hkv][B][D]
   const void* v_pool;
   int32_t T, R, D;
+  bool fp8;                    // E4M3 pools
   int32_t max_q_tiles;         // max over prefill requests of ceil(q_len * g / 128)
 };
 

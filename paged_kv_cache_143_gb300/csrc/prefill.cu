@@ -60,7 +60,7 @@ static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= kThreads * kLaunchRegs
               "register split exceeds the registers the block is launched with");
 static_assert(kRegsProducer % 8 == 0 && kRegsSoftmax % 8 == 0, "setmaxnreg takes multiples of 8");
 
-template <int D>
+template <int D, bool F8>
 struct Smem {
   static constexpr int kStages = D == 128 ? 2 : 4;     // KV tiles in flight
   static constexpr int kChunkBytes = kN * 128;         // 128 rows x 64 bf16 (one swizzle column)
@@ -70,7 +70,11 @@ struct Smem {
   static constexpr int kOffQ = 0;                      // Q_A, then Q_B
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+  // E4M3 pools: one staging tile of codes for K and for V, rows of D bytes
+  static constexpr int kK8Bytes = F8 ? kN * D : 0;
+  static constexpr int kOffK8 = kOffV + kStages * kKVBytes;
+  static constexpr int kOffV8 = kOffK8 + kK8Bytes;
+  static constexpr int kOffBar = kOffV8 + kK8Bytes;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kAlloc = kBytes + 1024;  // the base is rounded up to 1024 B
 };
@@ -85,6 +89,9 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t final_mma;
+  uint64_t k8_full, v8_full;    // E4M3 staging tile landed
+  uint64_t k8_empty, v8_empty;  // E4M3 staging tile converted
+  uint64_t q_conv;              // Q tiles converted to f16 (E4M3 pools)
   uint32_t tmem_base;
   int abort;
 };
@@ -99,12 +106,24 @@ __device__ __forceinline__ bool aborted(Bars* b) {
   return *reinterpret_cast<volatile int*>(&b->abort) != 0;
 }
 
-template <int D>
+// Widens 16 E4M3 codes to f16 (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& in, uint32_t (&out)[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(out[2 * i]), "=r"(out[2 * i + 1])
+        : "r"(w[i]));
+  }
+}
+
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_q,
                    const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, PrefillParams p) {
-  using S = Smem<D>;
+  using S = Smem<D, F8>;
   constexpr int kStages = S::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -149,11 +168,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->v_full[s], 1);
+      // bf16: completed by the TMA bytes; E4M3: by the two converter warps
+      mbar_init(&bars->k_full[s], F8 ? 2 : 1);
+      mbar_init(&bars->v_full[s], F8 ? 2 : 1);
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
+    mbar_init(&bars->k8_full, 1);
+    mbar_init(&bars->v8_full, 1);
+    mbar_init(&bars->k8_empty, 2);
+    mbar_init(&bars->v8_empty, 2);
+    mbar_init(&bars->q_conv, 8);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);  // one arrival per softmax warp
@@ -211,51 +236,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
       const int blk_lane = bad ? 0 : ids;  // a valid block; the output is then unspecified
       const int blk = __shfl_sync(full, blk_lane, box_block & 7);
-      const uint32_t bytes = (uint32_t)(nload * p.B * D * 2);
-      const bool issues = box_block < nload;
-      const int row = (blk * p.Hkv + kvh) * p.B;
-      const int dst_off = st * S::kKVBytes + box_chunk * S::kChunkBytes + box_block * p.B * 128;
-      // K of tile j: its stage is free once the S MMAs of tile j - kStages are done
+      const uint32_t bytes = (uint32_t)(nload * p.B * D * (F8 ? 1 : 2));
+      const bool issues = F8 ? lane < nload : box_block < nload;
+      const int row = ((F8 ? blk_lane : blk) * p.Hkv + kvh) * p.B;
+      const int dst_off =
+          F8 ? lane * p.B * D
+             : st * S::kKVBytes + box_chunk * S::kChunkBytes + box_block * p.B * 128;
+      uint64_t* kbar = F8 ? &bars->k8_full : &bars->k_full[st];
+      uint64_t* vbar = F8 ? &bars->v8_full : &bars->v_full[st];
+      // K of tile j: bf16 — its stage is free once the S MMAs of tile j - kStages
+      // are done; E4M3 — the staging tile is free once tile j - 1 is converted
       bool ok = true;
-      if (lane == 0 && j >= kStages)
+      if (F8 && lane == 0 && j >= 1) ok = mbar_wait(&bars->k8_empty, (j - 1) & 1, p.err);
+      if (!F8 && lane == 0 && j >= kStages)
         ok = mbar_wait(&bars->k_empty[st], ((j / kStages) - 1) & 1, p.err);
       if (!__shfl_sync(full, ok ? 1 : 0, 0) || aborted(bars)) {
         if (lane == 0) bars->abort = 1;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+      if (lane == 0) mbar_arrive_expect_tx(kbar, bytes);
       __syncwarp();
       if (issues)
-        tc::tma_load_2d(smem + S::kOffK + dst_off, &tmap_k, box_chunk * 64, row, &bars->k_full[st]);
+        tc::tma_load_2d(smem + (F8 ? S::kOffK8 : S::kOffK) + dst_off, &tmap_k,
+                        F8 ? 0 : box_chunk * 64, row, kbar);
       issued_k = j + 1;
-      // V of tile j: free once the PV MMAs of tile j - kStages are done
-      if (lane == 0 && j >= kStages)
+      // V of tile j: bf16 — free once the PV MMAs of tile j - kStages are done
+      if (F8 && lane == 0 && j >= 1) ok = mbar_wait(&bars->v8_empty, (j - 1) & 1, p.err);
+      if (!F8 && lane == 0 && j >= kStages)
         ok = mbar_wait(&bars->v_empty[st], ((j / kStages) - 1) & 1, p.err);
       if (!__shfl_sync(full, ok ? 1 : 0, 0)) {
         if (lane == 0) bars->abort = 1;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+      if (lane == 0) mbar_arrive_expect_tx(vbar, bytes);
       __syncwarp();
       if (issues)
-        tc::tma_load_2d(smem + S::kOffV + dst_off, &tmap_v, box_chunk * 64, row, &bars->v_full[st]);
+        tc::tma_load_2d(smem + (F8 ? S::kOffV8 : S::kOffV) + dst_off, &tmap_v,
+                        F8 ? 0 : box_chunk * 64, row, vbar);
       issued_v = j + 1;
       ids = next;
     }
     // every issued copy lands before the CTA may leave
     if (lane == 0) {
       mbar_wait(&bars->q_full, 0, p.err);
-      for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
-        mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err);
-      for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
-        mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err);
+      if (F8) {
+        if (issued_k > 0) mbar_wait(&bars->k8_full, (issued_k - 1) & 1, p.err);
+        if (issued_v > 0) mbar_wait(&bars->v8_full, (issued_v - 1) & 1, p.err);
+      } else {
+        for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
+          mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err);
+        for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
+          mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err);
+      }
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = tc::idesc_bf16_f32(kM, kN, false, false);
-      constexpr uint32_t idesc_o = tc::idesc_bf16_f32(kM, D, false, true);
-      bool ok = mbar_wait(&bars->q_full, 0, p.err);
+      constexpr uint32_t idesc_s = tc::idesc_16bit_f32(kM, kN, false, false, F8);
+      constexpr uint32_t idesc_o = tc::idesc_16bit_f32(kM, D, false, true, F8);
+      bool ok = mbar_wait(F8 ? &bars->q_conv : &bars->q_full, 0, p.err);
       auto issue_s = [&](int t, int j) {
         const uint8_t* qs = smem + S::kOffQ + t * S::kQBytes;
         const uint8_t* ks = smem + S::kOffK + (j % kStages) * S::kKVBytes;
@@ -310,6 +349,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mma_commit(&bars->final_mma);
       mbar_wait(&bars->final_mma, 0, p.err);
     }
+    } else if (F8) {
+    // ------------------------------------------ E4M3 -> f16 converters (warps 2, 3)
+    // Each 16-byte granule of codes (16 dims of one key) becomes two 16-byte
+    // f16 granules at their 128-byte-swizzled places in the K/V tile; keys at
+    // or past n_kv_all are written as zeros (so P = 0 never meets a NaN).
+    const int tid = threadIdx.x - 64;  // 0..63
+    constexpr int kGran = D / 16;       // granules of codes per key
+    auto convert = [&](const uint8_t* src, uint8_t* dst, int key0) {
+#pragma unroll 4
+      for (int G = tid; G < kN * kGran; G += 64) {
+        const int row = G / kGran, gq = G % kGran;
+        uint32_t h[8];
+        if (key0 + row < n_kv_all) {
+          const uint4 in = *reinterpret_cast<const uint4*>(src + row * D + gq * 16);
+          e4m3x16_to_f16(in, h);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) h[i] = 0u;
+        }
+        const int c = gq >> 2, q = 2 * (gq & 3);
+        uint8_t* line = dst + c * S::kChunkBytes + row * 128;
+        *reinterpret_cast<uint4*>(line + ((q ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(line + (((q + 1) ^ (row & 7)) << 4)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+      }
+    };
+    bool ok = true;
+    for (int j = 0; j < ntk_all && ok; ++j) {
+      const int st = j % kStages;
+      for (int kv = 0; kv < 2 && ok; ++kv) {
+        uint64_t* landed = kv ? &bars->v8_full : &bars->k8_full;
+        uint64_t* freed = kv ? &bars->v_empty[st] : &bars->k_empty[st];
+        ok = __all_sync(0xffffffffu, mbar_wait(landed, j & 1, p.err)) &&
+             (j < kStages ||
+              __all_sync(0xffffffffu, mbar_wait(freed, ((j / kStages) - 1) & 1, p.err))) &&
+             !aborted(bars);
+        if (!ok) break;
+        convert(smem + (kv ? S::kOffV8 : S::kOffK8),
+                smem + (kv ? S::kOffV : S::kOffK) + st * S::kKVBytes, j * kN);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
+          mbar_arrive(kv ? &bars->v8_empty : &bars->k8_empty);
+        }
+      }
+    }
+    if (!ok) bars->abort = 1;
     }
     // teardown: after every thread of the block is done with TMEM
     tc::fence_before_sync();
@@ -335,7 +422,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int limit = !valid_row ? 0 : (p.causal ? min(P + tok + 1, seq) : seq);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < my_ntk; ++j) {
+    float score_scale = p.scale_log2;  // log2(e) * scale (* k_scale for E4M3)
+    if (F8) {
+      // The MMAs run on f16 operands: this thread converts its own Q row in
+      // place, pre-scaled by 2^e so that the row's largest magnitude lands in
+      // [2^14, 2^15) (exact: a power of two), and divides the scores by 2^e.
+      if (my_ntk > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.err));
+        if (ok) {
+          uint8_t* qrow = smem + S::kOffQ + t * S::kQBytes + row * 128;
+          float amax = 0.f;
+#pragma unroll
+          for (int c = 0; c < S::kChunks; ++c)
+#pragma unroll
+            for (int gq = 0; gq < 8; ++gq) {
+              const uint4 v = *reinterpret_cast<const uint4*>(qrow + c * S::kChunkBytes + gq * 16);
+              float f[8];
+              bf16x8_to_f32(v, f);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+            }
+          int e2 = 0;
+          if (amax > 0.f) {
+            const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+            e2 = min(100, max(-120, 14 - ex));
+          }
+          const float up = __uint_as_float((uint32_t)(e2 + 127) << 23);
+          const float down = __uint_as_float((uint32_t)(127 - e2) << 23);
+          score_scale *= down;
+#pragma unroll
+          for (int c = 0; c < S::kChunks; ++c)
+#pragma unroll
+            for (int gq = 0; gq < 8; ++gq) {
+              uint4* ptr = reinterpret_cast<uint4*>(qrow + c * S::kChunkBytes + gq * 16);
+              float f[8];
+              bf16x8_to_f32(*ptr, f);
+              uint32_t h[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __half2 x = __floats2half2_rn(f[2 * e] * up, f[2 * e + 1] * up);
+                h[e] = *reinterpret_cast<uint32_t*>(&x);
+              }
+              *ptr = make_uint4(h[0], h[1], h[2], h[3]);
+            }
+          tc::fence_proxy_async_smem();
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_conv);
+    }
+    for (int j = 0; ok && j < my_ntk; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, p.err))) {
         ok = false;
         break;
@@ -364,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], s[k + u]);
       float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                        fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      mt *= p.scale_log2;
+      mt *= score_scale;
       float m_use = m_run, alpha = 1.f;
       bool rescale = false;
       if (m_run == -INFINITY) {
@@ -383,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < kN; k += 8)
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          s[k + u] = fast_exp2(fmaf(s[k + u], p.scale_log2, -m_sub));
+          s[k + u] = fast_exp2(fmaf(s[k + u], score_scale, -m_sub));
           sum[u] += s[k + u];
         }
       l_run = l_run * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
@@ -409,21 +545,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tmem_st32(tmem_o + c * 32, o);
         }
       }
-      // P as bf16 pairs over the first 64 columns of S_t (the A operand of PV)
+      // P as 16-bit pairs (bf16, or f16 for E4M3 pools) over the first 64
+      // columns of S_t (the A operand of PV)
 #pragma unroll
       for (int c = 0; c < kN / 64; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
-          w[k] = *reinterpret_cast<uint32_t*>(&h);
+          if (F8) {
+            __half2 h = __floats2half2_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+          } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(s[c * 64 + 2 * k], s[c * 64 + 2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+          }
         }
         tc::tmem_st32(tmem_s + c * 32, w);
       }
       tc::tmem_wait_st();
       // the CTA's last tile may hold keys past n_kv_all (unloaded blocks,
       // unwritten cells): zero those V rows so that P = 0 never meets a NaN
-      if (j == ntk_all - 1 && key0 + kN > n_kv_all) {
+      if (!F8 && j == ntk_all - 1 && key0 + kN > n_kv_all) {
         const int st = j % kStages;
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[st], (j / kStages) & 1, p.err))) {
           ok = false;
@@ -452,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) bars->abort = 1;
     if (ok && my_ntk > 0 && !aborted(bars)) {
       tc::fence_after_sync();
-      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+      const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
       __nv_bfloat16* orow = p.out + ((int64_t)(q_begin + tok) * p.Hq + kvh * g + head) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -496,7 +638,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
@@ -515,43 +657,46 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // K and V as rows [(block * Hkv + head) * B + offset][D]: box = 64 dims x B rows
+  // K and V as rows [(block * Hkv + head) * B + offset][D]. bf16: box = 64
+  // dims x B rows, 128-byte swizzled (the MMA operand layout); E4M3: box =
+  // D codes x B rows, unswizzled (the converter warps read it).
   {
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.num_blocks * p.Hkv * p.B};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)p.B};
+    cuuint64_t strides[1] = {(cuuint64_t)D * (F8 ? 1 : 2)};
+    cuuint32_t box[2] = {(cuuint32_t)(F8 ? D : 64), (cuuint32_t)p.B};
     cuuint32_t es[2] = {1, 1};
-    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(L.k_pool), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType dt =
+        F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapSwizzle sw = F8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (encode(&tk, dt, 2, const_cast<void*>(L.k_pool), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-    if (encode(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(L.v_pool), dims,
-               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (encode(&tv, dt, 2, const_cast<void*>(L.v_pool), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  constexpr int smem = Smem<D>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+  constexpr int smem = Smem<D, F8>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // the register split inside the kernel assumes the block is launched with
   // kLaunchRegs per thread; refuse to launch a build that allocated fewer
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, prefill_kernel<D>);
+  e = cudaFuncGetAttributes(&fa, prefill_kernel<D, F8>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
   dim3 grid((L.max_q_tiles + 1) / 2, p.Hkv, p.n_order ? p.n_order : L.R);  // tile pairs
-  prefill_kernel<D><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
+  prefill_kernel<D, F8><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s) {
-  if (L.D == 128) return launch_prefill_t<128>(L, s);
-  return launch_prefill_t<64>(L, s);
+  if (L.D == 128) return L.fp8 ? launch_prefill_t<128, true>(L, s) : launch_prefill_t<128, false>(L, s);
+  return L.fp8 ? launch_prefill_t<64, true>(L, s) : launch_prefill_t<64, false>(L, s);
 }
 
 }  // namespace pa

@@ -144,12 +144,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(const void* smem, uint32_t l
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulate.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
-  return (1u << 4)                       // D format: f32
-         | (1u << 7)                     // A format: bf16
-         | (1u << 10)                    // B format: bf16
+// Instruction descriptor for kind::f16 with A and B both bf16 (or both f16),
+// fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N, bool a_mn_major,
+                                                       bool b_mn_major, bool f16) {
+  return (1u << 4)                              // D format: f32
+         | ((f16 ? 0u : 1u) << 7)               // A format: f16 (0) or bf16 (1)
+         | ((f16 ? 0u : 1u) << 10)              // B format: the same as A
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

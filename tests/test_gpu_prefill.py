@@ -119,3 +119,39 @@ def test_prefill_is_deterministic(cuda_device):
     a = step.run().clone()
     b = step.run().clone()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+FP8_CASES = [
+    # seq_lens, q_lens, Hq, Hkv, D, B, causal
+    ([200], [200], 4, 4, 128, 16, 1),
+    ([300, 77], [45, 77], 8, 2, 128, 32, 1),
+    ([1000], [333], 16, 2, 128, 64, 1),
+    ([400], [150], 8, 4, 64, 16, 1),
+    ([250, 64], [250, 64], 4, 2, 128, 16, 0),
+    ([33, 1000, 17, 2048], [2, 1, 17, 600], 8, 2, 128, 16, 1),
+]
+
+
+@pytest.mark.parametrize("case", FP8_CASES, ids=[f"f{i}" for i in range(len(FP8_CASES))])
+def test_prefill_fp8_shapes(cuda_device, case):
+    """E4M3 pools: the oracle is fed the same codes (decoded, times the scales)."""
+    seq, ql, Hq, Hkv, D, B, causal = case
+    w = workloads.build(seq, ql, Hq, Hkv, D, B, kv_dtype="fp8", causal=causal,
+                        seed=sum(seq) + 7 * Hq + causal, device=cuda_device)
+    check(w, cuda_device)
+
+
+@pytest.mark.parametrize("q_mult", [0.001, 4.0, 300.0])
+def test_prefill_fp8_query_magnitudes(cuda_device, q_mult):
+    """The f16 operand path pre-scales each query row by a power of two: tiny
+    and large query magnitudes give the same accuracy."""
+    w = workloads.build([700, 900], [700, 300], Hq=8, Hkv=2, D=128, B=16, kv_dtype="fp8",
+                        seed=92, device=cuda_device, q_mult=q_mult)
+    check(w, cuda_device)
+
+
+@pytest.mark.slow
+def test_long_context_fp8_config_full_size(cuda_device):
+    w = workloads.make(5, device=cuda_device, kv_dtype="fp8")
+    rows = _sample_rows(w, 600, np.random.default_rng(6))
+    check(w, cuda_device, rows=rows)
