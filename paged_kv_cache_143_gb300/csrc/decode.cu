@@ -9,19 +9,23 @@
 // o_s,  o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s.
 //
 // Design (HBM-bound by construction):
-//  - one CTA per (key split, kv head [x head group], request): the GH query
-//    heads of a GQA group that share the kv head read the KV once;
-//  - warp 4 is a producer: one lane walks the block table and issues a 1-D
-//    bulk async copy (cp.async.bulk, completes on an mbarrier) per 16-key chunk
-//    of K and of V into an 8-stage shared-memory ring; a (block, kv head) is
-//    contiguous in the pool, so every chunk is one contiguous 16*D*elt copy;
-//  - warps 0..3 each own every 4th chunk and keep their own online-softmax
-//    state; lane (a, b) = (lane/8, lane%8) handles keys a, a+4, a+8, a+12 of the
-//    chunk and a fixed 1/8 of the head dimension, so a quarter-warp reads 128
-//    contiguous bytes of one key row (no bank conflicts); the dot product is
-//    finished with 3 xor-shuffles; P*V accumulates in registers and is reduced
-//    across the key lanes once per split;
-//  - the four warps merge through shared memory; one split writes bf16 output
+//  - one CTA per (key split, kv head, request): all g query heads of the GQA
+//    group that share the kv head are served from one read of the KV;
+//  - warp 4 is a producer: the warp fetches the block ids of 32 chunks at a
+//    time and one lane issues a 1-D bulk async copy (cp.async.bulk, completes
+//    on an mbarrier) per 16-key chunk of K and of V into an 8-stage shared
+//    ring; a (block, kv head) is contiguous in the pool, so every chunk is one
+//    contiguous 16*D*elt copy;
+//  - warps 0..3 compute. With g <= 4 each warp owns every 4th chunk for all
+//    g heads; with g = 8 (16) the warps split into 2 (4) head groups of 4
+//    heads and each chunk is consumed by one warp of every head group. Lane
+//    (a, b) = (lane/8, lane%8) handles keys a, a+4, a+8, a+12 of the chunk and
+//    a fixed 1/8 of the head dimension, so a quarter-warp reads 128
+//    contiguous bytes of one key row (no bank conflicts); the dot products
+//    use packed fp32 multiply-adds and finish with 3 xor-shuffles; P*V
+//    accumulates in registers and is reduced across the key lanes once per
+//    split;
+//  - the warps merge through shared memory; one split writes bf16 output
 //    directly, several write fp32 partials (o, m, l) for the merge kernel.
 // FP8 E4M3 codes are widened in registers (exact); k_scale is folded into the
 // query scale and v_scale into the output.
@@ -44,7 +48,9 @@ struct Geo {
   static constexpr int kPieceBytes = kRowBytes / 8 >= 16 ? 16 : kRowBytes / 8;
   static constexpr int kPieces = kRowBytes / (8 * kPieceBytes);
   static constexpr int kPieceElems = kPieceBytes / kElt;
+  static constexpr int kPiecePairs = kPieceElems / 2;
   static constexpr int kDimsPerLane = kPieces * kPieceElems;  // = D / 8
+  static constexpr int kPairsPerLane = kDimsPerLane / 2;
   static constexpr int kChunkBytes = kChunk * kRowBytes;
   static constexpr int kStageBytes = 2 * kChunkBytes;         // K then V
   static_assert(kDimsPerLane * 8 == D, "lane split must cover the head");
@@ -52,18 +58,24 @@ struct Geo {
   __device__ static constexpr int dim0(int p, int b) { return (p * 8 + b) * kPieceElems; }
 };
 
+// One piece of a key row as packed fp32 pairs (dims 2i, 2i+1).
 template <int D, bool FP8>
-__device__ __forceinline__ void load_piece(const uint8_t* src, float* f) {
+__device__ __forceinline__ void load_piece2(const uint8_t* src, uint64_t* f2) {
   using G = Geo<D, FP8>;
   if constexpr (!FP8) {
     const uint4 v = *reinterpret_cast<const uint4*>(src);
-    bf16x8_to_f32(v, f);
-  } else if constexpr (G::kPieceBytes == 16) {
-    const uint4 v = *reinterpret_cast<const uint4*>(src);
-    e4m3x16_to_f32(v, f);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f2[i] = f2_pack(bf16_lo(w[i]), bf16_hi(w[i]));
   } else {
-    const uint2 v = *reinterpret_cast<const uint2*>(src);
-    e4m3x8_to_f32(v, f);
+    float f[G::kPieceElems];
+    if constexpr (G::kPieceBytes == 16) {
+      e4m3x16_to_f32(*reinterpret_cast<const uint4*>(src), f);
+    } else {
+      e4m3x8_to_f32(*reinterpret_cast<const uint2*>(src), f);
+    }
+#pragma unroll
+    for (int i = 0; i < G::kPiecePairs; ++i) f2[i] = f2_pack(f[2 * i], f[2 * i + 1]);
   }
 }
 
@@ -73,14 +85,66 @@ struct SmemTail {
   int abort;
 };
 
-template <int D, bool FP8, int GH>
+// The producer warp of both decode kernels: the warp fetches the block ids of
+// 32 chunks at a time (lane i: chunk base + i, one coalesced load); lane 0
+// issues one bulk copy of K and one of V per 16-key chunk into the ring.
+template <class G>
+__device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
+                                        int r, int kvh, int k_begin, int nch, int lane) {
+  const unsigned full = 0xffffffffu;
+  const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
+  const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
+  int issued = 0;
+  bool ok = true;
+  for (int base = 0; base < nch && ok; base += 32) {
+    const int c_lane = base + lane;
+    const int key_lane = k_begin + c_lane * kChunk;
+    int blk_lane = c_lane < nch ? __ldg(table + key_lane / p.B) : 0;
+    const bool bad = c_lane < nch && (blk_lane < 0 || blk_lane >= p.num_blocks);
+    if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
+    if (bad) blk_lane = 0;  // read a valid block; the call's output is then unspecified
+    const int n = min(32, nch - base);
+    for (int i = 0; i < n; ++i) {
+      const int c = base + i;
+      const int blk = __shfl_sync(full, blk_lane, i);
+      if (lane == 0) {
+        const int stage = c % kStages, round = c / kStages;
+        if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
+          tail->abort = 1;
+          ok = false;
+        } else if (*reinterpret_cast<volatile int*>(&tail->abort)) {
+          ok = false;
+        } else {
+          const int key0 = k_begin + c * kChunk;
+          const int64_t off = ((int64_t)blk * p.Hkv + kvh) * head_stride +
+                              (int64_t)(key0 % p.B) * G::kRowBytes;
+          uint8_t* dst = ring + stage * G::kStageBytes;
+          mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
+          bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
+          bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
+          issued = c + 1;
+        }
+      }
+      ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+    }
+  }
+  // drain: every issued copy has landed before the CTA may exit
+  if (lane == 0)
+    for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
+      mbar_wait(&tail->full[c % kStages], (c / kStages) & 1, p.err);
+}
+
+// GH heads per warp, HG head groups per CTA (GH * HG = g).
+template <int D, bool FP8, int GH, int HG>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   using G = Geo<D, FP8>;
+  constexpr int CR = kConsumerWarps / HG;  // warps per head group (chunk residues)
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;                                               // kStages stages
+  uint8_t* ring = smem;                                                      // kStages stages
   float* comb_o = reinterpret_cast<float*>(smem + kStages * G::kStageBytes);  // [4][GH][D]
-  float* comb_m = comb_o + kConsumerWarps * GH * D;                   // [4][GH]
-  float* comb_l = comb_m + kConsumerWarps * GH;                       // [4][GH]
+  float* comb_m = comb_o + kConsumerWarps * GH * D;                          // [4][GH]
+  float* comb_l = comb_m + kConsumerWarps * GH;                              // [4][GH]
   SmemTail* tail = reinterpret_cast<SmemTail*>(comb_l + kConsumerWarps * GH);
 
   const int r = blockIdx.z;
@@ -101,15 +165,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   const int k_begin = split * p.split_tokens;
   const int k_end = min(seq, k_begin + p.split_tokens);
   const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
-  const int groups_per_kv = p.g / GH;
-  const int kvh = blockIdx.y / groups_per_kv;
-  const int h0 = kvh * p.g + (blockIdx.y % groups_per_kv) * GH;  // first query head
+  const int kvh = blockIdx.y;
+  const int hq0 = kvh * p.g;  // first query head of the group
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&tail->full[i], 1);
-      mbar_init(&tail->empty[i], 1);
+      mbar_init(&tail->empty[i], HG);  // one arrival per head group
     }
     tail->abort = 0;
     fence_mbar_init();
@@ -117,57 +180,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    // The warp fetches the block ids of 32 chunks at a time (lane i: chunk
-    // base + i, one coalesced load); lane 0 issues the bulk copies.
-    const unsigned full = 0xffffffffu;
-    const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
-    const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
-    int issued = 0;
-    bool ok = true;
-    for (int base = 0; base < nch && ok; base += 32) {
-      const int c_lane = base + lane;
-      const int key_lane = k_begin + c_lane * kChunk;
-      int blk_lane = c_lane < nch ? __ldg(table + key_lane / p.B) : 0;
-      const bool bad = c_lane < nch && (blk_lane < 0 || blk_lane >= p.num_blocks);
-      if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
-      if (bad) blk_lane = 0;  // read a valid block; the call's output is then unspecified
-      const int n = min(32, nch - base);
-      for (int i = 0; i < n; ++i) {
-        const int c = base + i;
-        const int blk = __shfl_sync(full, blk_lane, i);
-        if (lane == 0) {
-          const int stage = c % kStages, round = c / kStages;
-          if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
-            tail->abort = 1;
-            ok = false;
-          } else if (*reinterpret_cast<volatile int*>(&tail->abort)) {
-            ok = false;
-          } else {
-            const int key0 = k_begin + c * kChunk;
-            const int64_t off = ((int64_t)blk * p.Hkv + kvh) * head_stride +
-                                (int64_t)(key0 % p.B) * G::kRowBytes;
-            uint8_t* dst = ring + stage * G::kStageBytes;
-            mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
-            bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
-            bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
-            issued = c + 1;
-          }
-        }
-        ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-      }
-    }
-    // drain: every issued copy has landed before the CTA may exit
-    if (lane == 0)
-      for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
-        mbar_wait(&tail->full[c % kStages], (c / kStages) & 1, p.err);
+    produce<G>(p, ring, tail, r, kvh, k_begin, nch, lane);
     return;
   }
 
   // -------------------------------------------------------------- consumers
+  const int hg = warp % HG, cr = warp / HG;
+  const int h0 = hq0 + hg * GH;  // first query head of this warp
   const int a = lane >> 3, b = lane & 7;
-  float qf[GH][G::kDimsPerLane];
+  uint64_t q2[GH][G::kPairsPerLane];
   {
     const __nv_bfloat16* qrow = p.q + ((int64_t)qs * p.Hq + h0) * D;
 #pragma unroll
@@ -181,21 +202,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
           float f[8];
           bf16x8_to_f32(v, f);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) qf[h][pc * G::kPieceElems + e + x] = f[x] * p.q_scale;
+          for (int x = 0; x < 4; ++x)
+            q2[h][(pc * G::kPieceElems + e) / 2 + x] =
+                f2_pack(f[2 * x] * p.q_scale, f[2 * x + 1] * p.q_scale);
         }
   }
-  float o[GH][G::kDimsPerLane];
+  uint64_t o2[GH][G::kPairsPerLane];
   float m[GH], l[GH];
 #pragma unroll
   for (int h = 0; h < GH; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
-    for (int d = 0; d < G::kDimsPerLane; ++d) o[h][d] = 0.f;
+    for (int d = 0; d < G::kPairsPerLane; ++d) o2[h][d] = 0ull;
   }
 
   bool ok = true;
-  for (int c = warp; c < nch && ok; c += kConsumerWarps) {
+  for (int c = cr; c < nch && ok; c += CR) {
     const int stage = c % kStages, round = c / kStages;
     // every lane waits; the warp proceeds only if all lanes saw the data
     if (!__all_sync(0xffffffffu, mbar_wait(&tail->full[stage], round & 1, p.err))) {
@@ -211,17 +234,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint8_t* krow = Ks + (a + 4 * i) * G::kRowBytes;
+      uint64_t acc[GH];
 #pragma unroll
-      for (int h = 0; h < GH; ++h) s[i][h] = 0.f;
+      for (int h = 0; h < GH; ++h) acc[h] = 0ull;
 #pragma unroll
       for (int pc = 0; pc < G::kPieces; ++pc) {
-        float kf[G::kPieceElems];
-        load_piece<D, FP8>(krow + (pc * 8 + b) * G::kPieceBytes, kf);
+        uint64_t k2[G::kPiecePairs];
+        load_piece2<D, FP8>(krow + (pc * 8 + b) * G::kPieceBytes, k2);
 #pragma unroll
         for (int h = 0; h < GH; ++h)
 #pragma unroll
-          for (int e = 0; e < G::kPieceElems; ++e)
-            s[i][h] = fmaf(qf[h][pc * G::kPieceElems + e], kf[e], s[i][h]);
+          for (int e = 0; e < G::kPiecePairs; ++e)
+            acc[h] = f2_fma(q2[h][pc * G::kPiecePairs + e], k2[e], acc[h]);
+      }
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        float lo, hi;
+        f2_unpack(acc[h], lo, hi);
+        s[i][h] = lo + hi;
       }
     }
 #pragma unroll
@@ -255,8 +285,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
       }
       l[h] = l[h] * alpha + psum;
       m[h] = m_new;
+      const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-      for (int d = 0; d < G::kDimsPerLane; ++d) o[h][d] *= alpha;
+      for (int d = 0; d < G::kPairsPerLane; ++d) o2[h][d] = f2_mul(o2[h][d], a2);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -264,13 +295,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
       const uint8_t* vrow = Vs + (a + 4 * i) * G::kRowBytes;
 #pragma unroll
       for (int pc = 0; pc < G::kPieces; ++pc) {
-        float vf[G::kPieceElems];
-        load_piece<D, FP8>(vrow + (pc * 8 + b) * G::kPieceBytes, vf);
+        uint64_t v2[G::kPiecePairs];
+        load_piece2<D, FP8>(vrow + (pc * 8 + b) * G::kPieceBytes, v2);
 #pragma unroll
-        for (int h = 0; h < GH; ++h)
+        for (int h = 0; h < GH; ++h) {
+          const uint64_t p2 = f2_pack(s[i][h], s[i][h]);
 #pragma unroll
-          for (int e = 0; e < G::kPieceElems; ++e)
-            o[h][pc * G::kPieceElems + e] = fmaf(s[i][h], vf[e], o[h][pc * G::kPieceElems + e]);
+          for (int e = 0; e < G::kPiecePairs; ++e)
+            o2[h][pc * G::kPiecePairs + e] = f2_fma(p2, v2[e], o2[h][pc * G::kPiecePairs + e]);
+        }
       }
     }
     __syncwarp();
@@ -282,12 +315,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   for (int h = 0; h < GH; ++h) {
     l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
     l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
-#pragma unroll
-    for (int d = 0; d < G::kDimsPerLane; ++d) {
-      o[h][d] += __shfl_xor_sync(0xffffffffu, o[h][d], 8);
-      o[h][d] += __shfl_xor_sync(0xffffffffu, o[h][d], 16);
-    }
   }
+  float o[GH][G::kDimsPerLane];
+#pragma unroll
+  for (int h = 0; h < GH; ++h)
+#pragma unroll
+    for (int d = 0; d < G::kPairsPerLane; ++d) {
+      f2_unpack(o2[h][d], o[h][2 * d], o[h][2 * d + 1]);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        o[h][2 * d + x] += __shfl_xor_sync(0xffffffffu, o[h][2 * d + x], 8);
+        o[h][2 * d + x] += __shfl_xor_sync(0xffffffffu, o[h][2 * d + x], 16);
+      }
+    }
   if (a == 0) {
 #pragma unroll
     for (int h = 0; h < GH; ++h)
@@ -307,25 +347,344 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
 
   const int t = threadIdx.x;  // 0..127
-  for (int idx = t; idx < GH * D; idx += kConsumerWarps * 32) {
-    const int h = idx / D, d = idx % D;
+  for (int idx = t; idx < HG * GH * D; idx += kConsumerWarps * 32) {
+    const int hh = idx / D, d = idx % D;  // head within the group, dim
+    const int grp = hh / GH, h = hh % GH;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * GH + h]);
+    for (int k = 0; k < CR; ++k) M = fmaxf(M, comb_m[(grp + HG * k) * GH + h]);
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
+    for (int k = 0; k < CR; ++k) {
+      const int w = grp + HG * k;  // the warps of head group grp
       const float f = exp2f(comb_m[w * GH + h] - M);  // 0 for a warp with no chunk
       L += f * comb_l[w * GH + h];
       O += f * comb_o[(w * GH + h) * D + d];
     }
-    const int hq = h0 + h;
+    const int hq = hq0 + hh;
     if (nsplit == 1) {
       p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
     } else {
       const int64_t row = ((int64_t)r * p.Hq + hq) * p.ws_splits + split;
       p.ws_o[row * D + d] = O * p.v_scale;
       if (d == 0) p.ws_ml[row] = make_float2(M, L);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decode for GQA groups g >= 2 on warp-level tensor-core MMAs.
+//
+// Per kv head the decode contraction is [g x D] . [D x keys] with g <= 16,
+// below the smallest tcgen05 tile (M = 64), so each consumer warp issues
+// mma.sync m16n8k16 (f32 accumulate) on register fragments: the g query
+// heads are the 16 rows (padded with zero rows), a 16-key chunk is two n8
+// tiles. The operands come straight from the linear rows the bulk copies
+// deliver:
+//  - S = Q K^T: a fixed permutation of the head dimension, the same for Q and
+//    K, maps k-steps 2j and 2j+1 of lane (grp, tig) onto the 8 contiguous
+//    dims 32 j + 8 tig .. +7, so every K fragment is one 16-byte load of
+//    key row grp (bf16), or one 8-byte load widened to f16 (E4M3);
+//  - P is the S accumulator tile re-packed to 16 bits (no data movement);
+//  - O += P V: output dim 16 grp + nt (D = 128; 8 grp + nt for D = 64) is
+//    column grp of n-tile nt, so lane (grp, tig) reads rows 2tig, 2tig+1,
+//    2tig+8, 2tig+9 over its 16 (8) contiguous dims and pairs them with prmt.
+// E4M3 pools run f16 MMAs: the codes widen exactly to f16, and each query row
+// is pre-scaled by a power of two into [2^14, 2^15) before its f16 rounding
+// (undone in the score scale), so f16 range never limits the queries.
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p) {
+  using G = Geo<D, FP8>;
+  constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
+  constexpr int KJ = D / 32;       // pairs of k-steps
+  constexpr int DG = D / 8;        // output dims per lane group = n-tiles of O
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  float* comb_o = reinterpret_cast<float*>(smem + kStages * G::kStageBytes);  // [4][16][D]
+  float* comb_m = comb_o + kConsumerWarps * kRows * D;                       // [4][16]
+  float* comb_l = comb_m + kConsumerWarps * kRows;                           // [4][16]
+  SmemTail* tail = reinterpret_cast<SmemTail*>(comb_l + kConsumerWarps * kRows);
+
+  const int r = blockIdx.z;
+  const int qs = p.qsl[r];
+  if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
+  const int seq = p.seq_lens[r];
+  if (seq < 1 || seq > p.max_blocks * p.B) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int nsplit = (seq + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit > (int)gridDim.x) {  // device seq_lens disagree with the host mirror
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int split = blockIdx.x;
+  if (split >= nsplit) return;
+  const int k_begin = split * p.split_tokens;
+  const int k_end = min(seq, k_begin + p.split_tokens);
+  const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
+  const int kvh = blockIdx.y;
+  const int g = p.g;
+  const int hq0 = kvh * g;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->empty[i], 1);
+    }
+    tail->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kConsumerWarps) {
+    produce<G>(p, ring, tail, r, kvh, k_begin, nch, lane);
+    return;
+  }
+
+  const int grp = lane >> 2, tig = lane & 3;
+  const unsigned full = 0xffffffffu;
+  // ---- Q fragments: qa[j][row][w] = the 16-bit pair of dims 32j + 8tig + 2w
+  uint32_t qa[KJ][2][4];
+  float sc[2];  // score scale of rows grp and grp + 8 (log2 units)
+  {
+    float qf[2][KJ][8];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+      const int row = grp + 8 * ri;
+#pragma unroll
+      for (int j = 0; j < KJ; ++j) {
+        if (row < g) {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+              p.q + ((int64_t)qs * p.Hq + hq0 + row) * D + 32 * j + 8 * tig));
+          bf16x8_to_f32(v, qf[ri][j]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) qf[ri][j][e] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+      float up = 1.f;
+      sc[ri] = p.q_scale;
+      if (FP8) {
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < KJ; ++j)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(qf[ri][j][e]));
+        amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+        int e2 = 0;
+        if (amax > 0.f) {
+          const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+          e2 = min(100, max(-120, 14 - ex));
+        }
+        up = __uint_as_float((uint32_t)(e2 + 127) << 23);
+        sc[ri] *= __uint_as_float((uint32_t)(127 - e2) << 23);
+      }
+#pragma unroll
+      for (int j = 0; j < KJ; ++j)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          if (FP8) {
+            __half2 h = __floats2half2_rn(qf[ri][j][2 * w] * up, qf[ri][j][2 * w + 1] * up);
+            qa[j][ri][w] = *reinterpret_cast<uint32_t*>(&h);
+          } else {
+            __nv_bfloat162 h = __floats2bfloat162_rn(qf[ri][j][2 * w], qf[ri][j][2 * w + 1]);
+            qa[j][ri][w] = *reinterpret_cast<uint32_t*>(&h);
+          }
+        }
+    }
+  }
+  auto mma = [](float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                uint32_t b1) {
+    if (FP8)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+          "{%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  };
+  // 8 consecutive elements of a row -> four 16-bit pairs
+  auto load8 = [](const uint8_t* src, uint32_t (&w)[4]) {
+    if (FP8) {
+      const uint2 v = *reinterpret_cast<const uint2*>(src);
+      asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+          "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+          "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+          : "r"(v.x), "r"(v.y));
+    } else {
+      const uint4 v = *reinterpret_cast<const uint4*>(src);
+      w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+    }
+  };
+
+  float o[DG][4];
+#pragma unroll
+  for (int nt = 0; nt < DG; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+
+  bool ok = true;
+  for (int c = warp; c < nch && ok; c += kConsumerWarps) {
+    const int stage = c % kStages, round = c / kStages;
+    if (!__all_sync(full, mbar_wait(&tail->full[stage], round & 1, p.err))) {
+      tail->abort = 1;
+      ok = false;
+      break;
+    }
+    const uint8_t* Ks = ring + stage * G::kStageBytes;
+    const uint8_t* Vs = Ks + G::kChunkBytes;
+    const int key0 = k_begin + c * kChunk;
+
+    // S for keys 8t + grp (B fragments), t = n-tile
+    float s[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
+      const uint8_t* krow = Ks + (8 * t + grp) * G::kRowBytes;
+#pragma unroll
+      for (int j = 0; j < KJ; ++j) {
+        uint32_t kw[4];
+        load8(krow + (32 * j + 8 * tig) * G::kElt, kw);
+        mma(s[t], qa[j][0][0], qa[j][1][0], qa[j][0][1], qa[j][1][1], kw[0], kw[1]);
+        mma(s[t], qa[j][0][2], qa[j][1][2], qa[j][0][3], qa[j][1][3], kw[2], kw[3]);
+      }
+    }
+    // scale, mask, online softmax of rows grp (c0, c1) and grp + 8 (c2, c3)
+    float alpha[2];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float& x = s[t][2 * ri + e];
+          x = key0 + 8 * t + 2 * tig + e < k_end ? x * sc[ri] : -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
+      const float m_new = fmaxf(m[ri], mx);
+      alpha[ri] = exp2f(m[ri] - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float& x = s[t][2 * ri + e];
+          x = exp2f(x - m_new);
+          ps += x;
+        }
+      l[ri] = l[ri] * alpha[ri] + ps;
+      m[ri] = m_new;
+    }
+    if (__any_sync(full, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+      for (int nt = 0; nt < DG; ++nt) {
+        o[nt][0] *= alpha[0];
+        o[nt][1] *= alpha[0];
+        o[nt][2] *= alpha[1];
+        o[nt][3] *= alpha[1];
+      }
+    }
+    // P as the A fragment of the 16-key step
+    uint32_t pa[4];
+    {
+      auto pk = [](float x, float y) -> uint32_t {
+        if (FP8) {
+          __half2 h = __floats2half2_rn(x, y);
+          return *reinterpret_cast<uint32_t*>(&h);
+        }
+        __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+        return *reinterpret_cast<uint32_t*>(&h);
+      };
+      pa[0] = pk(s[0][0], s[0][1]);
+      pa[1] = pk(s[0][2], s[0][3]);
+      pa[2] = pk(s[1][0], s[1][1]);
+      pa[3] = pk(s[1][2], s[1][3]);
+    }
+    // V rows 2tig, 2tig+1, 2tig+8, 2tig+9 over dims DG grp .. DG grp + DG - 1
+    uint32_t vw[4][DG / 2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int kr = 2 * tig + (i & 1) + 8 * (i >> 1);
+      const uint8_t* vrow = Vs + kr * G::kRowBytes + DG * grp * G::kElt;
+#pragma unroll
+      for (int h = 0; h < DG / 8; ++h) {
+        uint32_t w4[4];
+        load8(vrow + 8 * h * G::kElt, w4);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
+      }
+      if (key0 + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
+#pragma unroll
+        for (int w = 0; w < DG / 2; ++w) vw[i][w] = 0u;
+    }
+#pragma unroll
+    for (int nt = 0; nt < DG; ++nt) {
+      const uint32_t sel = (nt & 1) ? 0x7632u : 0x5410u;
+      uint32_t b0, b1;
+      asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b0) : "r"(vw[0][nt >> 1]), "r"(vw[1][nt >> 1]), "r"(sel));
+      asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b1) : "r"(vw[2][nt >> 1]), "r"(vw[3][nt >> 1]), "r"(sel));
+      mma(o[nt], pa[0], pa[1], pa[2], pa[3], b0, b1);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->empty[stage]);
+  }
+
+  // per-row sums over the four lanes of a row
+#pragma unroll
+  for (int ri = 0; ri < 2; ++ri) {
+    l[ri] += __shfl_xor_sync(full, l[ri], 1);
+    l[ri] += __shfl_xor_sync(full, l[ri], 2);
+  }
+#pragma unroll
+  for (int ri = 0; ri < 2; ++ri) {
+    const int row = grp + 8 * ri;
+    if (row < g) {
+#pragma unroll
+      for (int nt = 0; nt < DG; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          comb_o[(warp * kRows + row) * D + DG * (2 * tig + e) + nt] = o[nt][2 * ri + e];
+      if (tig == 0) {
+        comb_m[warp * kRows + row] = m[ri];
+        comb_l[warp * kRows + row] = l[ri];
+      }
+    }
+  }
+  named_bar_sync(1, kConsumerWarps * 32);
+  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
+
+  for (int idx = threadIdx.x; idx < g * D; idx += kConsumerWarps * 32) {
+    const int row = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * kRows + row]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) {
+      const float f = exp2f(comb_m[w * kRows + row] - M);  // 0 for a warp with no chunk
+      L += f * comb_l[w * kRows + row];
+      O += f * comb_o[(w * kRows + row) * D + d];
+    }
+    const int hq = hq0 + row;
+    if (nsplit == 1) {
+      p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
+    } else {
+      const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + split;
+      p.ws_o[orow * D + d] = O * p.v_scale;
+      if (d == 0) p.ws_ml[orow] = make_float2(M, L);
     }
   }
 }
@@ -360,39 +719,48 @@ constexpr int decode_smem_bytes() {
          (int)sizeof(SmemTail);
 }
 
-template <int D, bool FP8, int GH>
+template <int D, bool FP8, int GH, int HG>
 cudaError_t launch_decode_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
   constexpr int smem = decode_smem_bytes<D, FP8, GH>();
-  auto k = decode_kernel<D, FP8, GH>;
+  auto k = decode_kernel<D, FP8, GH, HG>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(max_splits, p.Hkv * (p.g / GH), R);
+  dim3 grid(max_splits, p.Hkv, R);
   k<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 template <int D, bool FP8>
-cudaError_t launch_decode_d(const DecodeParams& p, int GH, int R, int max_splits,
-                            cudaStream_t s) {
-  switch (GH) {
-    case 1: return launch_decode_t<D, FP8, 1>(p, R, max_splits, s);
-    case 2: return launch_decode_t<D, FP8, 2>(p, R, max_splits, s);
-    default: return launch_decode_t<D, FP8, 4>(p, R, max_splits, s);
-  }
+cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
+  constexpr int smem =
+      kStages * Geo<D, FP8>::kStageBytes + kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
+  auto k = decode_mma_kernel<D, FP8>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(max_splits, p.Hkv, R);
+  k<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// g = 1: one head per kv head, CUDA-core dot products (a 16-row MMA would be
+// 1/16 used); g >= 2: warp-level tensor-core MMAs for all g heads at once.
+template <int D, bool FP8>
+cudaError_t launch_decode_d(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
+  if (p.g == 1) return launch_decode_t<D, FP8, 1, 1>(p, R, max_splits, s);
+  if (p.g == 2 || p.g == 4 || p.g == 8 || p.g == 16)
+    return launch_decode_mma_t<D, FP8>(p, R, max_splits, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int decode_heads_per_cta(int g) { return g < 4 ? g : 4; }
-
 cudaError_t launch_decode(const DecodeParams& p, int D, bool fp8, int R, int max_splits,
                           cudaStream_t s) {
-  const int GH = decode_heads_per_cta(p.g);
   if (D == 128)
-    return fp8 ? launch_decode_d<128, true>(p, GH, R, max_splits, s)
-               : launch_decode_d<128, false>(p, GH, R, max_splits, s);
-  return fp8 ? launch_decode_d<64, true>(p, GH, R, max_splits, s)
-             : launch_decode_d<64, false>(p, GH, R, max_splits, s);
+    return fp8 ? launch_decode_d<128, true>(p, R, max_splits, s)
+               : launch_decode_d<128, false>(p, R, max_splits, s);
+  return fp8 ? launch_decode_d<64, true>(p, R, max_splits, s)
+             : launch_decode_d<64, false>(p, R, max_splits, s);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int D, int R, cudaStream_t s) {

@@ -101,8 +101,7 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
     // least 256 keys, a multiple of the 16-key chunk; bounded by the splits
     // the workspace can hold. Depends only on seq_lens, never on placement.
-    const int gh = pa::decode_heads_per_cta(g);
-    const int64_t head_groups = (int64_t)Hkv * (g / gh);
+    const int64_t head_groups = Hkv;  // one CTA per kv head serves all g query heads
     const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
     int64_t split = (dec_keys * head_groups + target_ctas - 1) / target_ctas;
     if (split < 256) split = 256;

@@ -28,9 +28,6 @@ struct DecodeParams {
   unsigned* err;
 };
 
-// Query heads handled by one decode CTA for GQA group size g.
-int decode_heads_per_cta(int g);
-
 constexpr int kMaxOrderedPrefill = 256;
 
 struct PrefillParams {
