@@ -38,7 +38,7 @@ namespace {
 
 constexpr int kChunk = 16;         // keys per pipeline stage
 constexpr int kConsumerWarps = 4;  // warps 0..3 compute, warp 4 produces
-constexpr int kStages = 8;         // ring depth (a multiple of kConsumerWarps)
+constexpr int kMaxStages = 16;     // ring depth of the E4M3 kernels
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 template <int D, bool FP8>
@@ -53,6 +53,12 @@ struct Geo {
   static constexpr int kPairsPerLane = kDimsPerLane / 2;
   static constexpr int kChunkBytes = kChunk * kRowBytes;
   static constexpr int kStageBytes = 2 * kChunkBytes;         // K then V
+  // ring depth: 64 KB of K/V in flight per CTA whatever the element size
+  // (8 stages of bf16 chunks, 16 of E4M3 chunks for D = 128); a multiple of
+  // the consumer warp count
+  static constexpr int kStages = 65536 / kStageBytes > kMaxStages ? kMaxStages
+                                                                  : 65536 / kStageBytes;
+  static_assert(kStages % kConsumerWarps == 0, "ring depth");
   static_assert(kDimsPerLane * 8 == D, "lane split must cover the head");
   // first dimension of piece p of lane b
   __device__ static constexpr int dim0(int p, int b) { return (p * 8 + b) * kPieceElems; }
@@ -80,8 +86,8 @@ __device__ __forceinline__ void load_piece2(const uint8_t* src, uint64_t* f2) {
 }
 
 struct SmemTail {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   int abort;
 };
 
@@ -108,7 +114,7 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
       const int c = base + i;
       const int blk = __shfl_sync(full, blk_lane, i);
       if (lane == 0) {
-        const int stage = c % kStages, round = c / kStages;
+        const int stage = c % G::kStages, round = c / G::kStages;
         if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
           tail->abort = 1;
           ok = false;
@@ -131,14 +137,15 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
   }
   // drain: every issued copy has landed before the CTA may exit
   if (lane == 0)
-    for (int c = issued - kStages > 0 ? issued - kStages : 0; c < issued; ++c)
-      mbar_wait(&tail->full[c % kStages], (c / kStages) & 1, p.err);
+    for (int c = issued - G::kStages > 0 ? issued - G::kStages : 0; c < issued; ++c)
+      mbar_wait(&tail->full[c % G::kStages], (c / G::kStages) & 1, p.err);
 }
 
 // GH heads per warp, HG head groups per CTA (GH * HG = g).
 template <int D, bool FP8, int GH, int HG>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   using G = Geo<D, FP8>;
+  constexpr int kStages = G::kStages;
   constexpr int CR = kConsumerWarps / HG;  // warps per head group (chunk residues)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;                                                      // kStages stages
@@ -395,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 template <int D, bool FP8>
 __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p) {
   using G = Geo<D, FP8>;
+  constexpr int kStages = G::kStages;
   constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
   constexpr int KJ = D / 32;       // pairs of k-steps
   constexpr int DG = D / 8;        // output dims per lane group = n-tiles of O
@@ -715,7 +723,7 @@ __global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
 
 template <int D, bool FP8, int GH>
 constexpr int decode_smem_bytes() {
-  return kStages * Geo<D, FP8>::kStageBytes + kConsumerWarps * GH * (D + 2) * 4 +
+  return Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes + kConsumerWarps * GH * (D + 2) * 4 +
          (int)sizeof(SmemTail);
 }
 
@@ -732,8 +740,8 @@ cudaError_t launch_decode_t(const DecodeParams& p, int R, int max_splits, cudaSt
 
 template <int D, bool FP8>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
-  constexpr int smem =
-      kStages * Geo<D, FP8>::kStageBytes + kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
+  constexpr int smem = Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
+                       kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
   auto k = decode_mma_kernel<D, FP8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
