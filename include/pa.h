@@ -259,6 +259,16 @@ pa_status pa_forward_noalloc(const void* q, void* out, const int32_t* query_star
                              int32_t causal, int32_t max_splits, pa_stream_t stream);
 
 /*
+ * pa_selftest_wait_timeout — diagnostics, not part of the method on the pages.
+ * Launches one small kernel that waits on a device barrier which nothing will
+ * complete, through the same bounded wait that every kernel of this library
+ * uses. The wait gives up after its limit (about 2 seconds), records the
+ * timeout in the error word and returns: afterwards pa_get_error() reports
+ * PA_ERR_TIMEOUT. Lets callers and tests check the no-hang error path.
+ */
+pa_status pa_selftest_wait_timeout(pa_stream_t stream);
+
+/*
  * pa_kernel_launches — number of CUDA kernels this library has launched in
  * this process (all devices, all streams), for launch accounting in
  * benchmarks and tests. Not part of the method on the pages; never fails.

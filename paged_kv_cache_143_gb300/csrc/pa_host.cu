@@ -2,6 +2,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace {
@@ -92,4 +93,26 @@ extern "C" const char* pa_status_string(pa_status status) {
 
 extern "C" uint64_t pa_kernel_launches(void) {
   return g_launches.load(std::memory_order_relaxed);
+}
+
+namespace {
+// Waits on a barrier that nothing completes, through the bounded wait every
+// kernel of the library uses: it gives up after pa::kWaitLimitNs, records
+// kErrTimeout and returns.
+__global__ void wait_timeout_kernel(unsigned* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    pa::mbar_init(&bar, 1);
+    pa::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) pa::mbar_wait(&bar, 0, err);
+}
+}  // namespace
+
+extern "C" pa_status pa_selftest_wait_timeout(pa_stream_t stream) {
+  unsigned* err = pa::error_word();
+  if (!err) return PA_ERR_CUDA;
+  wait_timeout_kernel<<<1, 32, 0, pa::as_stream(stream)>>>(err);
+  return pa::launch_status();
 }

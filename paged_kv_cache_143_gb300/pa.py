@@ -24,7 +24,7 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
            "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
-           "pa_forward_noalloc")
+           "pa_forward_noalloc", "pa_selftest_wait_timeout")
 
 
 class PaError(RuntimeError):
@@ -72,6 +72,8 @@ def lib():
         L.pa_forward_noalloc.restype = ctypes.c_int
         L.pa_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32, I32,
                                          I32, P]
+        L.pa_selftest_wait_timeout.restype = ctypes.c_int
+        L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_kernel_launches.restype = ctypes.c_uint64
         L.pa_kernel_launches.argtypes = []
         _lib = L
@@ -216,6 +218,12 @@ def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor, stream=None)
     st = lib().pa_copy_blocks(ctypes.byref(pool.struct()), _dptr(src, torch.int32),
                               _dptr(dst, torch.int32), src.numel(), _stream(stream))
     _check(st, "pa_copy_blocks")
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Runs the library's bounded device wait on a barrier nothing completes
+    (about 2 s); pa_get_error() afterwards reports PA_ERR_TIMEOUT."""
+    _check(lib().pa_selftest_wait_timeout(_stream(stream)), "pa_selftest_wait_timeout")
 
 
 def get_error(stream=None) -> int:
