@@ -250,7 +250,10 @@ def run_libpa(args):
     del step
     torch.cuda.empty_cache()
     line["mixed_batch"] = run_mixed(args, dev, 3)
-    line["long_context"] = {"bf16": run_mixed(args, dev, 5, "bf16")}
+    line["long_context"] = {"bf16": run_mixed(args, dev, 5, "bf16"),
+                            "fp8": run_mixed(args, dev, 5, "fp8")}
+    line["prefix_shared"] = run_prefix_shared(args, dev)
+    line["tiny_decode"] = run_tiny(args, dev)
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(line), flush=True)
@@ -327,6 +330,44 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
         "decode_only": {"ms": round(ms_dec, 4), "kv_bytes": int(dec_bytes),
                         "gbs": round(dec_bytes / (ms_dec * 1e-3) / 1e9, 1)},
     }
+
+
+def run_prefix_shared(args, dev):
+    """Prefix-shared parallel sampling (8 groups x 16 samples, FP8 KV): decode
+    step time, logical KV bytes (what every request reads) and unique KV bytes
+    (shared prompt blocks counted once)."""
+    import torch
+    import workloads
+    from paged_kv_cache_143_gb300 import accounting, pa
+    stream = torch.cuda.current_stream()
+    w = workloads.make(4, device=dev)
+    step = Step(w, dev, max_splits=32)
+    ms = timed(step.run, args.steps, args.warmup, stream)
+    fwd = lambda: pa.forward(step.q, step.out, step.qsl, step.seq, w.qsl, w.seq_lens,
+                             step.gathered, step.pool, w.scale, w.causal, workspace=step.ws)
+    ms_fwd = timed(fwd, args.steps, args.warmup, stream)
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the prefix-shared step")
+    logical = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    unique = accounting.unique_kv_bytes(w.tables, w.seq_lens, w.B, w.Hkv, w.D, w.elt_bytes)
+    peak, _ = load_peaks()
+    del step
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "ms_per_step": round(ms, 4), "forward_ms": round(ms_fwd, 4),
+            "logical_kv_bytes": int(logical), "unique_kv_bytes": int(unique),
+            "effective_gbs": round(logical / (ms_fwd * 1e-3) / 1e9, 1),
+            "unique_gbs": round(unique / (ms_fwd * 1e-3) / 1e9, 1),
+            "unique_frac_of_hbm": round(unique / (ms_fwd * 1e-3) / 1e9 / peak, 4)}
+
+
+def run_tiny(args, dev):
+    """The tiny decode batch (4 requests): latency of one step, in microseconds."""
+    import torch
+    import workloads
+    w = workloads.make(1, device=dev)
+    step = Step(w, dev, max_splits=8)
+    us = timed(step.run, max(args.steps, 20), args.warmup, torch.cuda.current_stream()) * 1e3
+    return {"workload": w.name, "us_per_step": round(us, 2)}
 
 
 def load_peaks_tensor():
