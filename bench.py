@@ -145,13 +145,25 @@ class Step:
         n = pa.forward_workspace_size(w.R, w.Hq, w.D, max_splits)
         self.ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
 
-    def run(self):
+    def run(self, cascade=False):
         pa, w = self.pa, self.w
         pa.apply_staged_writes(self.table, self.rows, self.starts, self.offs, self.vals,
                                self.idx, self.gathered)
         pa.write_kv(self.pool, self.new_k, self.new_v, self.slots)
-        pa.forward(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens, self.gathered,
-                   self.pool, w.scale, w.causal, workspace=self.ws)
+        self.forward(cascade)
+
+    def forward(self, cascade=False):
+        pa, w = self.pa, self.w
+        if cascade:  # groups of consecutive requests sharing their prompt blocks
+            first = [min(m) for m in w.groups]
+            size = [len(m) for m in w.groups]
+            prefix_blocks = [p // w.B for p in w.group_prefix]
+            pa.forward_shared_prefix(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens,
+                                     self.gathered, self.pool, w.scale, first, size,
+                                     prefix_blocks, causal=w.causal, workspace=self.ws)
+        else:
+            pa.forward(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens, self.gathered,
+                       self.pool, w.scale, w.causal, workspace=self.ws)
 
 
 def run_libpa(args):
@@ -277,6 +289,26 @@ def timed(fn, steps, warmup, stream):
     return a.elapsed_time(b) / steps
 
 
+def timed_flushed(fn, steps, warmup, stream):
+    """Mean ms of fn() over `steps` calls after `warmup`, each call timed alone
+    by CUDA events on `stream` after a 512 MB write that evicts L2 (for
+    workloads whose inputs fit in the 129 MB L2)."""
+    import torch
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=torch.cuda.current_device())
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush.fill_(1)
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
 def run_mixed(args, dev, cfg, kv_dtype=None):
     """Mixed decode + prefill step of config `cfg` (tokens/s of the whole step),
     and the prefill kernel alone on the same chunks (causal TFLOP/s)."""
@@ -335,29 +367,32 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
 def run_prefix_shared(args, dev):
     """Prefix-shared parallel sampling (8 groups x 16 samples, FP8 KV): decode
     step time, logical KV bytes (what every request reads) and unique KV bytes
-    (shared prompt blocks counted once)."""
+    (shared prompt blocks counted once); through pa_forward (every request
+    reads its whole context) and through pa_forward_shared_prefix (each
+    group's prompt read once)."""
     import torch
     import workloads
     from paged_kv_cache_143_gb300 import accounting, pa
     stream = torch.cuda.current_stream()
     w = workloads.make(4, device=dev)
     step = Step(w, dev, max_splits=32)
-    ms = timed(step.run, args.steps, args.warmup, stream)
-    fwd = lambda: pa.forward(step.q, step.out, step.qsl, step.seq, w.qsl, w.seq_lens,
-                             step.gathered, step.pool, w.scale, w.causal, workspace=step.ws)
-    ms_fwd = timed(fwd, args.steps, args.warmup, stream)
-    if pa.get_error() != pa.PA_OK:
-        raise RuntimeError("device error in the prefix-shared step")
     logical = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
     unique = accounting.unique_kv_bytes(w.tables, w.seq_lens, w.B, w.Hkv, w.D, w.elt_bytes)
     peak, _ = load_peaks()
+    res = {"workload": w.name, "logical_kv_bytes": int(logical), "unique_kv_bytes": int(unique)}
+    res["l2"] = "flushed before every timed call (unique KV < 129 MB)"
+    for key, cascade in (("pa_forward", False), ("shared_prefix", True)):
+        ms = timed_flushed(lambda: step.run(cascade), args.steps, args.warmup, stream)
+        ms_fwd = timed_flushed(lambda: step.forward(cascade), args.steps, args.warmup, stream)
+        if pa.get_error() != pa.PA_OK:
+            raise RuntimeError("device error in the prefix-shared step")
+        res[key] = {"ms_per_step": round(ms, 4), "forward_ms": round(ms_fwd, 4),
+                    "effective_gbs": round(logical / (ms_fwd * 1e-3) / 1e9, 1),
+                    "unique_gbs": round(unique / (ms_fwd * 1e-3) / 1e9, 1),
+                    "unique_frac_of_hbm": round(unique / (ms_fwd * 1e-3) / 1e9 / peak, 4)}
     del step
     torch.cuda.empty_cache()
-    return {"workload": w.name, "ms_per_step": round(ms, 4), "forward_ms": round(ms_fwd, 4),
-            "logical_kv_bytes": int(logical), "unique_kv_bytes": int(unique),
-            "effective_gbs": round(logical / (ms_fwd * 1e-3) / 1e9, 1),
-            "unique_gbs": round(unique / (ms_fwd * 1e-3) / 1e9, 1),
-            "unique_frac_of_hbm": round(unique / (ms_fwd * 1e-3) / 1e9 / peak, 4)}
+    return res
 
 
 def run_tiny(args, dev):

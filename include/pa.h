@@ -162,6 +162,55 @@ pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
                      pa_stream_t stream);
 
 /*
+ * pa_forward_shared_prefix — pa_forward for a batch in which groups of decode
+ * requests share the physical blocks of a common prefix (parallel sampling,
+ * beam candidates, a shared system prompt).
+ * [vLLM-wiki, "블록 공유와 쓰기 시 복사"]:
+ * the samples of one prompt map the prompt's logical blocks to the same
+ * physical blocks (reference-counted, copied on write); only the tails differ.
+ * The result is the attention pa_forward computes (the same bounds against
+ * exact arithmetic; the fp32 summation order differs): the softmax over the
+ * union of the prefix keys and the tail keys is taken in parts, the prefix
+ * pieces and the tail splits, merged by log-sum-exp. Each group's prefix K/V
+ * is read once for all of its members (a tensor-core tile whose rows are the
+ * members' decode tokens x the GQA heads) instead of once per member.
+ *
+ * Arguments as pa_forward, plus:
+ *   num_groups          G, 0 <= G <= 64 (more: PA_ERR_UNSUPPORTED). G == 0
+ *                       behaves as pa_forward.
+ *   group_first_host    host int32 [G]: group k is the group_size_host[k]
+ *   group_size_host     host int32 [G]  consecutive requests from
+ *                       group_first_host[k]; groups in increasing order and
+ *                       disjoint, within [0, num_reqs); other requests may sit
+ *                       before, between and after them
+ *   prefix_blocks_host  host int32 [G]: the first prefix_blocks_host[k]
+ *                       entries of every member's block-table row are the
+ *                       same physical blocks (the caller's contract: the
+ *                       prefix is read through the first member's row)
+ *   workspace           required: at least pa_forward_workspace_size(R, Hq,
+ *                       head_dim, 2) bytes (one prefix piece and one tail
+ *                       split per member); more lets the call cut prefixes and
+ *                       tails into more pieces that run in parallel
+ *
+ * Host checks (PA_ERR_INVALID): every member is a decode request (q_len 1)
+ * with seq_len > prefix_blocks * block_size, 1 <= prefix_blocks <=
+ * max_blocks, groups non-empty and in range, workspace large enough.
+ * Requests outside every group, and prefill chunks, are handled exactly as by
+ * pa_forward. If members' rows differ on the prefix, the result is
+ * unspecified but every block id read is still bounds-checked.
+ */
+pa_status pa_forward_shared_prefix(const void* q, void* out, const int32_t* query_start_loc,
+                                   const int32_t* seq_lens, const int32_t* qsl_host,
+                                   const int32_t* seq_lens_host, const int32_t* block_tables,
+                                   int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                                   int32_t num_q_heads, const pa_kv_pool* pool, float scale,
+                                   int32_t causal, int32_t num_groups,
+                                   const int32_t* group_first_host,
+                                   const int32_t* group_size_host,
+                                   const int32_t* prefix_blocks_host, void* workspace,
+                                   size_t workspace_bytes, pa_stream_t stream);
+
+/*
  * pa_apply_staged_writes — apply packed block-table diffs, then gather the
  * rows of this step.
  * [MRV2, "재설계 3: 큰 block table은 staged diff만 보낸다"]: the device copy of the

@@ -162,14 +162,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
     return;
   }
-  const int nsplit = (seq + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit > (int)gridDim.x) {  // device seq_lens disagree with the host mirror
+  // keys [k_lo, seq): all of them, or the private tail after a shared prefix
+  const int grp_id = group_of(p.groups, r);
+  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
+  const int slot0 = prefix_slots(p.groups, grp_id);  // a member's prefix pieces come first
+  if (k_lo >= seq) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit > (int)gridDim.x || (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
+    // device seq_lens disagree with the host mirror
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
     return;
   }
   const int split = blockIdx.x;
   if (split >= nsplit) return;
-  const int k_begin = split * p.split_tokens;
+  const int k_begin = k_lo + split * p.split_tokens;
   const int k_end = min(seq, k_begin + p.split_tokens);
   const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
   const int kvh = blockIdx.y;
@@ -369,10 +378,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
       O += f * comb_o[(w * GH + h) * D + d];
     }
     const int hq = hq0 + hh;
-    if (nsplit == 1) {
+    if (slot0 + nsplit == 1) {
       p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
     } else {
-      const int64_t row = ((int64_t)r * p.Hq + hq) * p.ws_splits + split;
+      const int64_t row = ((int64_t)r * p.Hq + hq) * p.ws_splits + slot0 + split;
       p.ws_o[row * D + d] = O * p.v_scale;
       if (d == 0) p.ws_ml[row] = make_float2(M, L);
     }
@@ -421,14 +430,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
     return;
   }
-  const int nsplit = (seq + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit > (int)gridDim.x) {  // device seq_lens disagree with the host mirror
+  // keys [k_lo, seq): all of them, or the private tail after a shared prefix
+  const int grp_id = group_of(p.groups, r);
+  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
+  const int slot0 = prefix_slots(p.groups, grp_id);  // a member's prefix pieces come first
+  if (k_lo >= seq) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit > (int)gridDim.x || (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
+    // device seq_lens disagree with the host mirror
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
     return;
   }
   const int split = blockIdx.x;
   if (split >= nsplit) return;
-  const int k_begin = split * p.split_tokens;
+  const int k_begin = k_lo + split * p.split_tokens;
   const int k_end = min(seq, k_begin + p.split_tokens);
   const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
   const int kvh = blockIdx.y;
@@ -687,10 +705,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
       O += f * comb_o[(w * kRows + row) * D + d];
     }
     const int hq = hq0 + row;
-    if (nsplit == 1) {
+    if (slot0 + nsplit == 1) {
       p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
     } else {
-      const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + split;
+      const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + slot0 + split;
       p.ws_o[orow * D + d] = O * p.v_scale;
       if (d == 0) p.ws_ml[orow] = make_float2(M, L);
     }
@@ -706,7 +724,12 @@ __global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
   if (p.qsl[r + 1] - qs != 1) return;
   const int seq = p.seq_lens[r];
   if (seq < 1 || seq > p.max_blocks * p.B) return;
-  const int nsplit = (seq + p.split_tokens - 1) / p.split_tokens;
+  const int grp_id = group_of(p.groups, r);
+  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
+  if (k_lo >= seq) return;
+  // slots: the shared-prefix partial (group members) and the splits
+  const int nsplit =
+      prefix_slots(p.groups, grp_id) + (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
   if (nsplit <= 1 || nsplit > p.ws_splits) return;
   const int64_t row0 = ((int64_t)r * p.Hq + h) * p.ws_splits;
   float M = -INFINITY;

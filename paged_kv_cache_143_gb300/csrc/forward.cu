@@ -29,13 +29,23 @@ extern "C" size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_head
   return split_row_bytes(num_reqs, num_q_heads, head_dim) * (size_t)max_splits;
 }
 
-extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
-                                const int32_t* seq_lens, const int32_t* qsl_host,
-                                const int32_t* seq_lens_host, const int32_t* block_tables,
-                                int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
-                                int32_t num_q_heads, const pa_kv_pool* pool, float scale,
-                                int32_t causal, void* workspace, size_t workspace_bytes,
-                                pa_stream_t stream) {
+namespace {
+
+// Optional groups of decode requests that share their first blocks.
+struct Cascade {
+  int32_t n;
+  const int32_t* first_host;          // [n]
+  const int32_t* size_host;           // [n]
+  const int32_t* prefix_blocks_host;  // [n]
+};
+
+pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
+                       const int32_t* seq_lens, const int32_t* qsl_host,
+                       const int32_t* seq_lens_host, const int32_t* block_tables,
+                       int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                       int32_t num_q_heads, const pa_kv_pool* pool, float scale, int32_t causal,
+                       const Cascade* cas, void* workspace, size_t workspace_bytes,
+                       pa_stream_t stream) {
   pa_status st = pa::check_pool(pool);
   if (st != PA_OK) return st;
   const int R = num_reqs, T = num_tokens, Hq = num_q_heads;
@@ -46,7 +56,11 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
   if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return PA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_INVALID;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID;
-  if (R == 0) return T == 0 ? PA_OK : PA_ERR_INVALID;
+  if (cas && cas->n < 0) return PA_ERR_INVALID;
+  if (cas && cas->n > pa::kMaxGroups) return PA_ERR_UNSUPPORTED;
+  if (cas && cas->n > 0 && (!cas->first_host || !cas->size_host || !cas->prefix_blocks_host))
+    return PA_ERR_INVALID;
+  if (R == 0) return T == 0 && (!cas || cas->n == 0) ? PA_OK : PA_ERR_INVALID;
   if (!qsl_host || !seq_lens_host || !query_start_loc || !seq_lens || !block_tables)
     return PA_ERR_INVALID;
   if (T > 0 && (!q || !out || !pa::aligned16(q) || !pa::aligned16(out))) return PA_ERR_INVALID;
@@ -54,87 +68,88 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
 
   // ---- plan from the host mirrors
   if (qsl_host[0] != 0 || qsl_host[R] != T) return PA_ERR_INVALID;
-  int n_dec = 0, n_pre = 0, max_dec_seq = 0, max_q_tiles = 0;
-  int64_t dec_keys = 0;
+  int n_pre = 0, max_q_tiles = 0;
   for (int r = 0; r < R; ++r) {
     const int ql = qsl_host[r + 1] - qsl_host[r];
     if (ql < 0) return PA_ERR_INVALID;
     if (ql == 0) continue;
     const int seq = seq_lens_host[r];
     if (seq < ql || (int64_t)seq > (int64_t)max_blocks * B) return PA_ERR_INVALID;
-    if (ql == 1) {
-      ++n_dec;
-      dec_keys += seq;
-      if (seq > max_dec_seq) max_dec_seq = seq;
-    } else {
+    if (ql > 1) {
       ++n_pre;
       const int tiles = (ql + 128 / g - 1) / (128 / g);
       if (tiles > max_q_tiles) max_q_tiles = tiles;
     }
   }
   if (R > 65535) return PA_ERR_UNSUPPORTED;
+
+  // ---- shared-prefix groups: consecutive decode requests, each with keys
+  // past the prefix
+  pa::GroupDesc gd{};
+  int max_prefix = 0, max_members = 0;
+  if (cas && cas->n > 0) {
+    gd.n = cas->n;
+    int prev_end = 0;
+    for (int k = 0; k < cas->n; ++k) {
+      const int a = cas->first_host[k], n = cas->size_host[k];
+      const int pb = cas->prefix_blocks_host[k];
+      if (a < prev_end || n < 1 || (int64_t)a + n > R || pb < 1 || pb > max_blocks)
+        return PA_ERR_INVALID;
+      prev_end = a + n;
+      const int pt = pb * B;
+      for (int r = a; r < a + n; ++r)
+        if (qsl_host[r + 1] - qsl_host[r] != 1 || seq_lens_host[r] <= pt) return PA_ERR_INVALID;
+      gd.first[k] = a;
+      gd.size[k] = n;
+      gd.prefix_tokens[k] = pt;
+      max_prefix = std::max(max_prefix, pt);
+      max_members = std::max(max_members, n);
+    }
+  }
+  const size_t row_bytes = split_row_bytes(R, Hq, D);
+  const int64_t ws_splits = row_bytes ? (int64_t)(workspace_bytes / row_bytes) : 0;
+  // the pieces of a prefix and at least one tail split each need a slot
+  if (gd.n > 0 && ws_splits < 2) return PA_ERR_INVALID;
+  int pieces = 0, pairs_per_piece = 0;
+  if (gd.n > 0) {
+    // enough prefix CTAs to fill the GPU once, each piece at least 512 keys
+    const int tiles = (max_members + 128 / g - 1) / (128 / g);
+    pairs_per_piece = (tiles + 1) / 2;
+    const int64_t ctas = (int64_t)gd.n * Hkv * pairs_per_piece;
+    int64_t want = std::max<int64_t>(1, pa::num_sms() / ctas);
+    want = std::min<int64_t>(want, (max_prefix + 511) / 512);
+    want = std::min<int64_t>(want, ws_splits - 1);
+    gd.prefix_split_tokens = round_up((int)((max_prefix + want - 1) / want), 128);
+    pieces = (max_prefix + gd.prefix_split_tokens - 1) / gd.prefix_split_tokens;
+  }
+  // decode key range of request r: [k_lo, seq)
+  auto group_slots = [&](int r, int* k_lo) {
+    const int k = pa::group_of(gd, r);
+    *k_lo = k >= 0 ? gd.prefix_tokens[k] : 0;
+    return pa::prefix_slots(gd, k);
+  };
+  int n_dec = 0, max_dec_len = 0;
+  int64_t dec_keys = 0;
+  for (int r = 0; r < R; ++r) {
+    if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+    int k_lo;
+    group_slots(r, &k_lo);
+    const int len = seq_lens_host[r] - k_lo;
+    ++n_dec;
+    dec_keys += len;
+    max_dec_len = std::max(max_dec_len, len);
+  }
+
   unsigned* err = pa::error_word();
   if (!err) return PA_ERR_CUDA;
   cudaStream_t s = pa::as_stream(stream);
   const bool fp8 = pool->dtype == PA_KV_FP8_E4M3;
   const float kLog2e = 1.4426950408889634f;
+  float* ws_o = static_cast<float*>(workspace);
+  float2* ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
+                                            (size_t)R * Hq * ws_splits * D * 4);
 
-  if (n_dec > 0) {
-    pa::DecodeParams p{};
-    p.q = static_cast<const __nv_bfloat16*>(q);
-    p.out = static_cast<__nv_bfloat16*>(out);
-    p.qsl = query_start_loc;
-    p.seq_lens = seq_lens;
-    p.block_tables = block_tables;
-    p.max_blocks = max_blocks;
-    p.Hq = Hq;
-    p.Hkv = Hkv;
-    p.g = g;
-    p.k_pool = static_cast<const uint8_t*>(pool->k_pool);
-    p.v_pool = static_cast<const uint8_t*>(pool->v_pool);
-    p.num_blocks = pool->num_blocks;
-    p.B = B;
-    p.q_scale = scale * kLog2e * (fp8 ? pool->k_scale : 1.f);
-    p.v_scale = fp8 ? pool->v_scale : 1.f;
-    p.err = err;
-
-    // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
-    // least 256 keys, a multiple of the 16-key chunk; bounded by the splits
-    // the workspace can hold. Depends only on seq_lens, never on placement.
-    const int64_t head_groups = Hkv;  // one CTA per kv head serves all g query heads
-    const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
-    int64_t split = (dec_keys * head_groups + target_ctas - 1) / target_ctas;
-    if (split < 256) split = 256;
-    if (split > max_dec_seq) split = max_dec_seq;
-    split = round_up((int)split, 16);
-    const size_t row_bytes = split_row_bytes(R, Hq, D);
-    const int64_t ws_splits = row_bytes ? (int64_t)(workspace_bytes / row_bytes) : 0;
-    int max_splits = (int)((max_dec_seq + split - 1) / split);
-    if (max_splits > 1 && max_splits > ws_splits) {
-      if (ws_splits <= 1) {
-        split = round_up(max_dec_seq, 16);
-      } else {
-        split = round_up((int)((max_dec_seq + ws_splits - 1) / ws_splits), 16);
-      }
-      max_splits = (int)((max_dec_seq + split - 1) / split);
-    }
-    if (max_splits > 65535) return PA_ERR_UNSUPPORTED;
-    p.split_tokens = (int)split;
-    p.ws_splits = max_splits > 1 ? (int)ws_splits : 1;
-    if (max_splits > 1) {
-      p.ws_o = static_cast<float*>(workspace);
-      p.ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
-                                          (size_t)R * Hq * ws_splits * D * 4);
-    }
-    if (pa::launch_decode(p, D, fp8, R, max_splits, s) != cudaSuccess) return PA_ERR_CUDA;
-    pa::count_launches(1);
-    if (max_splits > 1) {
-      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
-      pa::count_launches(1);
-    }
-  }
-
-  if (n_pre > 0) {
+  auto prefill_launch = [&]() {
     pa::PrefillLaunch L{};
     L.p.out = static_cast<__nv_bfloat16*>(out);
     L.p.qsl = query_start_loc;
@@ -157,6 +172,99 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     L.T = T;
     L.R = R;
     L.D = D;
+    return L;
+  };
+
+  if (n_dec > 0) {
+    pa::DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.qsl = query_start_loc;
+    p.seq_lens = seq_lens;
+    p.block_tables = block_tables;
+    p.max_blocks = max_blocks;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = g;
+    p.k_pool = static_cast<const uint8_t*>(pool->k_pool);
+    p.v_pool = static_cast<const uint8_t*>(pool->v_pool);
+    p.num_blocks = pool->num_blocks;
+    p.B = B;
+    p.q_scale = scale * kLog2e * (fp8 ? pool->k_scale : 1.f);
+    p.v_scale = fp8 ? pool->v_scale : 1.f;
+    p.err = err;
+    p.groups = gd;
+
+    // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
+    // least 256 keys, a multiple of the 16-key chunk; bounded by the slots
+    // the workspace holds (a group member's prefix pieces take the first
+    // ones). Depends only on seq_lens and the groups, never on placement.
+    const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
+    int64_t split = (dec_keys * Hkv + target_ctas - 1) / target_ctas;
+    split = std::max<int64_t>(split, 256);
+    split = std::min<int64_t>(split, max_dec_len);
+    split = round_up((int)split, 16);
+    auto plan = [&](int64_t sp, int* grid_x) {
+      int need = 0, gx = 0;
+      for (int r = 0; r < R; ++r) {
+        if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+        int k_lo;
+        const int slot0 = group_slots(r, &k_lo);
+        const int n = (int)((seq_lens_host[r] - k_lo + sp - 1) / sp);
+        gx = std::max(gx, n);
+        need = std::max(need, slot0 + n);
+      }
+      *grid_x = gx;
+      return need;
+    };
+    int grid_x;
+    int need = plan(split, &grid_x);
+    if (need > 1 && need > ws_splits) {
+      if (ws_splits <= 1) {  // no groups here: one split per request, no workspace
+        split = round_up(max_dec_len, 16);
+      } else {
+        int64_t sp = 16;
+        for (int r = 0; r < R; ++r) {
+          if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+          int k_lo;
+          const int free_slots = (int)ws_splits - group_slots(r, &k_lo);
+          sp = std::max<int64_t>(sp, (seq_lens_host[r] - k_lo + free_slots - 1) / free_slots);
+        }
+        split = round_up((int)sp, 16);
+      }
+      need = plan(split, &grid_x);
+    }
+    if (grid_x > 65535) return PA_ERR_UNSUPPORTED;
+    p.split_tokens = (int)split;
+    p.ws_splits = need > 1 ? (int)ws_splits : 1;
+    if (need > 1) {
+      p.ws_o = ws_o;
+      p.ws_ml = ws_ml;
+    }
+    if (gd.n > 0) {  // the prefix pieces of every group, into slots 0..pieces-1
+      pa::PrefillLaunch L = prefill_launch();
+      L.p.mode = 1;
+      L.p.causal = 0;
+      L.p.groups = gd;
+      L.p.pairs_per_piece = pairs_per_piece;
+      L.p.ws_o = ws_o;
+      L.p.ws_ml = ws_ml;
+      L.p.ws_splits = (int)ws_splits;
+      L.max_q_tiles = 2 * pairs_per_piece;
+      L.pieces = pieces;
+      if (pa::launch_prefill(L, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+    }
+    if (pa::launch_decode(p, D, fp8, R, grid_x, s) != cudaSuccess) return PA_ERR_CUDA;
+    pa::count_launches(1);
+    if (need > 1) {
+      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+    }
+  }
+
+  if (n_pre > 0) {
+    pa::PrefillLaunch L = prefill_launch();
     L.max_q_tiles = max_q_tiles;
     // launch the requests with the most causal (query, key) pairs first so
     // that their long-running tiles do not form the tail of the grid
@@ -178,4 +286,32 @@ extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_s
     pa::count_launches(1);
   }
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, const int32_t* qsl_host,
+                                const int32_t* seq_lens_host, const int32_t* block_tables,
+                                int32_t max_blocks, int32_t num_reqs, int32_t num_tokens,
+                                int32_t num_q_heads, const pa_kv_pool* pool, float scale,
+                                int32_t causal, void* workspace, size_t workspace_bytes,
+                                pa_stream_t stream) {
+  return forward_impl(q, out, query_start_loc, seq_lens, qsl_host, seq_lens_host, block_tables,
+                      max_blocks, num_reqs, num_tokens, num_q_heads, pool, scale, causal,
+                      nullptr, workspace, workspace_bytes, stream);
+}
+
+extern "C" pa_status pa_forward_shared_prefix(
+    const void* q, void* out, const int32_t* query_start_loc, const int32_t* seq_lens,
+    const int32_t* qsl_host, const int32_t* seq_lens_host, const int32_t* block_tables,
+    int32_t max_blocks, int32_t num_reqs, int32_t num_tokens, int32_t num_q_heads,
+    const pa_kv_pool* pool, float scale, int32_t causal, int32_t num_groups,
+    const int32_t* group_first_host, const int32_t* group_size_host,
+    const int32_t* prefix_blocks_host, void* workspace, size_t workspace_bytes,
+    pa_stream_t stream) {
+  const Cascade c{num_groups, group_first_host, group_size_host, prefix_blocks_host};
+  return forward_impl(q, out, query_start_loc, seq_lens, qsl_host, seq_lens_host, block_tables,
+                      max_blocks, num_reqs, num_tokens, num_q_heads, pool, scale, causal, &c,
+                      workspace, workspace_bytes, stream);
 }

@@ -8,6 +8,35 @@
 
 namespace pa {
 
+// Groups of consecutive decode requests whose first blocks are shared.
+constexpr int kMaxGroups = 64;
+struct GroupDesc {
+  int32_t n;                          // number of groups (0: none)
+  int32_t first[kMaxGroups];          // group k = requests [first[k], first[k] + size[k]),
+  int32_t size[kMaxGroups];           //   increasing and disjoint
+  int32_t prefix_tokens[kMaxGroups];  // shared prefix length (whole blocks)
+  // the prefix is cut into pieces of this many keys (a multiple of 128);
+  // piece i of a member's prefix lands in split slot i, its tail after them
+  int32_t prefix_split_tokens;
+};
+
+// Group of request r (-1 if none), by binary search over the group starts.
+__host__ __device__ inline int group_of(const GroupDesc& gd, int r) {
+  if (gd.n == 0 || r < gd.first[0]) return -1;
+  int lo = 0, hi = gd.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (gd.first[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  return r < gd.first[lo] + gd.size[lo] ? lo : -1;
+}
+
+// Split slots that a group member's prefix pieces take (0 if ungrouped).
+__host__ __device__ inline int prefix_slots(const GroupDesc& gd, int grp) {
+  return grp < 0 ? 0
+                 : (gd.prefix_tokens[grp] + gd.prefix_split_tokens - 1) / gd.prefix_split_tokens;
+}
+
 struct DecodeParams {
   const __nv_bfloat16* q;      // [T][Hq][D]
   __nv_bfloat16* out;          // [T][Hq][D]
@@ -26,6 +55,10 @@ struct DecodeParams {
   float* ws_o;                 // [R][Hq][ws_splits][D] unnormalised partial outputs
   float2* ws_ml;               // [R][Hq][ws_splits] (max in log2 units, sum)
   unsigned* err;
+  // requests in a group attend only to their keys after the shared prefix
+  // (key range [prefix_tokens, seq_len)) and always write partials into
+  // split slots 1.. (slot 0 holds the prefix partial)
+  GroupDesc groups;
 };
 
 constexpr int kMaxOrderedPrefill = 256;
@@ -46,6 +79,16 @@ struct PrefillParams {
   // grid.z walks every request in batch order
   int32_t n_order;
   int32_t order[kMaxOrderedPrefill];
+  // mode 1: the CTAs of blockIdx.z = k attend the decode tokens of group k's
+  // members (consecutive tokens) to its shared prefix [0, prefix_tokens),
+  // non-causally, and write fp32 partials (o, max, sum) into slot 0 of the
+  // decode workspace instead of bf16 output
+  int32_t mode;
+  int32_t pairs_per_piece;  // mode 1: blockIdx.x = piece * pairs_per_piece + tile pair
+  GroupDesc groups;
+  float* ws_o;
+  float2* ws_ml;
+  int32_t ws_splits;
 };
 
 struct PrefillLaunch {
@@ -56,6 +99,7 @@ struct PrefillLaunch {
   int32_t T, R, D;
   bool fp8;                    // E4M3 pools
   int32_t max_q_tiles;         // max over prefill requests of ceil(q_len * g / 128)
+  int32_t pieces;              // mode 1: prefix pieces per group (grid x = pieces * pairs)
 };
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s);

@@ -24,7 +24,7 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
            "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
-           "pa_forward_noalloc", "pa_selftest_wait_timeout")
+           "pa_forward_noalloc", "pa_selftest_wait_timeout", "pa_forward_shared_prefix")
 
 
 class PaError(RuntimeError):
@@ -72,6 +72,9 @@ def lib():
         L.pa_forward_noalloc.restype = ctypes.c_int
         L.pa_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32, I32,
                                          I32, P]
+        L.pa_forward_shared_prefix.restype = ctypes.c_int
+        L.pa_forward_shared_prefix.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32,
+                                               I32, I32, P, P, P, P, SZ, P]
         L.pa_selftest_wait_timeout.restype = ctypes.c_int
         L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_kernel_launches.restype = ctypes.c_uint64
@@ -172,6 +175,44 @@ def forward(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
         Hq, ctypes.byref(pool.struct()), float(scale), int(causal), ws_ptr, ws_bytes,
         _stream(stream))
     _check(st, "pa_forward")
+
+
+MAX_PREFIX_GROUPS = 64  # groups accepted by pa_forward_shared_prefix
+
+
+def forward_shared_prefix(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
+                          seq_lens: torch.Tensor, qsl_host, seq_lens_host,
+                          block_tables: torch.Tensor, pool: KVPool, scale: float,
+                          group_first_host, group_size_host, prefix_blocks_host,
+                          causal: int = 1, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """pa_forward where group k, the group_size_host[k] consecutive decode
+    requests from group_first_host[k], shares the first prefix_blocks_host[k]
+    block-table entries. The workspace is required (room for at least two
+    splits per request)."""
+    qh = _host_i32(qsl_host)
+    sh = _host_i32(seq_lens_host)
+    gf = _host_i32(group_first_host)
+    gn = _host_i32(group_size_host)
+    pb = _host_i32(prefix_blocks_host)
+    R = sh.size
+    if qh.size != R + 1:
+        raise ValueError("qsl_host must have num_reqs + 1 entries")
+    G = pb.size
+    if gf.size != G or gn.size != G:
+        raise ValueError("group arrays must have num_groups entries each")
+    T, Hq, D = q.shape
+    max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    ws_ptr = _dptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    host = lambda a: a.ctypes.data_as(ctypes.c_void_p) if G > 0 else None
+    st = lib().pa_forward_shared_prefix(
+        _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
+        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
+        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), G, host(gf), host(gn),
+        host(pb), ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "pa_forward_shared_prefix")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20  # PA_NOALLOC_SCRATCH_BYTES in include/pa.h

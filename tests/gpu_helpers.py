@@ -57,15 +57,36 @@ class DeviceStep:
         nbytes = pa.forward_workspace_size(w.R, w.Hq, w.D, max_splits) if max_splits else 0
         self.ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev) if nbytes else None
 
-    def run(self, tables=None):
+    def run(self, tables=None, cascade=False):
+        """cascade: attention through pa_forward_shared_prefix with the
+        workload's groups (consecutive requests) and their prefix blocks."""
         w = self.w
         pa.apply_staged_writes(self.table, self.rows, self.starts, self.offs, self.vals,
                                self.idx, self.gathered)
         pa.write_kv(self.pool, self.new_k, self.new_v, self.slots)
-        pa.forward(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens,
-                   self.gathered if tables is None else tables, self.pool, w.scale, w.causal,
-                   workspace=self.ws)
+        tab = self.gathered if tables is None else tables
+        if cascade:
+            first, size, prefix_blocks = group_arrays(w)
+            pa.forward_shared_prefix(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens,
+                                     tab, self.pool, w.scale, first, size, prefix_blocks,
+                                     causal=w.causal, workspace=self.ws)
+        else:
+            pa.forward(self.q, self.out, self.qsl, self.seq, w.qsl, w.seq_lens, tab, self.pool,
+                       w.scale, w.causal, workspace=self.ws)
         return self.out
+
+
+def group_arrays(w):
+    """(first [G], size [G], prefix_blocks [G]) of a workload whose groups
+    are runs of consecutive requests, sorted by their first member."""
+    rows = []
+    for members, pt in zip(w.groups, w.group_prefix):
+        m = sorted(members)
+        assert m == list(range(m[0], m[0] + len(m))), "group members must be consecutive"
+        rows.append((m[0], len(m), pt // w.B))
+    rows.sort()
+    a = np.array(rows, np.int32).reshape(-1, 3)
+    return a[:, 0].copy(), a[:, 1].copy(), a[:, 2].copy()
 
 
 def oracle_step(w, rows=None):

@@ -50,3 +50,37 @@ def test_status_strings_and_host_side_rejections():
 def test_workspace_size_formula():
     assert pa.forward_workspace_size(256, 32, 128, 4) == 256 * 32 * 4 * (128 * 4 + 8)
     assert pa.forward_workspace_size(0, 32, 128, 4) == 0
+
+
+def test_shared_prefix_host_rejections():
+    """Group arguments of pa_forward_shared_prefix are checked on the host
+    before any CUDA call (fake, aligned device pointers are never touched)."""
+    import numpy as np
+    L = pa.lib()
+    pool = pa._Pool(16, 16, 32, 16, 4, 64, 0, 1.0, 1.0)
+    i32 = lambda *v: np.array(v, np.int32)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+
+    def call(qsl, seq, first, size, prefix, G=None, ws_bytes=1 << 20):
+        G = len(first) if G is None else G
+        R = len(seq)
+        return L.pa_forward_shared_prefix(
+            16, 16, 16, 16, ptr(qsl), ptr(seq), 16, 4, R, int(qsl[-1]), 4, ctypes.byref(pool),
+            0.125, 1, G, ptr(first), ptr(size), ptr(prefix), 16 if ws_bytes else None, ws_bytes,
+            None)
+
+    qsl, seq = i32(0, 1, 2, 3), i32(40, 50, 60)
+    assert call(qsl, seq, i32(0), i32(2), i32(2), G=65) == pa.PA_ERR_UNSUPPORTED
+    assert call(qsl, seq, i32(0), i32(2), i32(3)) == pa.PA_ERR_INVALID  # seq 40 <= prefix 48
+    assert call(qsl, seq, i32(0), i32(2), i32(0)) == pa.PA_ERR_INVALID  # empty prefix
+    assert call(qsl, seq, i32(0), i32(2), i32(5)) == pa.PA_ERR_INVALID  # prefix > max_blocks
+    assert call(qsl, seq, i32(0), i32(0), i32(2)) == pa.PA_ERR_INVALID  # empty group
+    assert call(qsl, seq, i32(2), i32(2), i32(2)) == pa.PA_ERR_INVALID  # past num_reqs
+    assert call(qsl, seq, i32(0, 1), i32(2, 2), i32(2, 2)) == pa.PA_ERR_INVALID  # overlap
+    assert call(qsl, seq, i32(1, 0), i32(1, 1), i32(2, 2)) == pa.PA_ERR_INVALID  # unordered
+    assert call(qsl, seq, i32(-1), i32(2), i32(2)) == pa.PA_ERR_INVALID
+    assert call(i32(0, 1, 2, 5), seq, i32(1), i32(2), i32(1)) == pa.PA_ERR_INVALID  # a prefill
+    # one prefix piece and one tail split per request do not fit in no workspace
+    assert call(qsl, seq, i32(0), i32(2), i32(2), ws_bytes=0) == pa.PA_ERR_INVALID
+    one_split = pa.forward_workspace_size(3, 4, 64, 1)
+    assert call(qsl, seq, i32(0), i32(2), i32(2), ws_bytes=one_split) == pa.PA_ERR_INVALID

@@ -56,6 +56,7 @@ class Workload:
     diff_val_offsets: np.ndarray  # int32 [W+1]
     diff_vals: np.ndarray  # int32 [N]
     groups: List[List[int]] = field(default_factory=list)
+    group_prefix: List[int] = field(default_factory=list)  # shared prefix tokens per group
     seed: int = 0
 
     @property
@@ -233,7 +234,8 @@ def build(seq_lens: Sequence[int], q_lens: Sequence[int], Hq: int, Hkv: int, D: 
         new_k=new_k, new_v=new_v, slot_mapping=torch.from_numpy(new_slots).to(device),
         k_scale=k_scale, v_scale=v_scale, max_reqs=mr, table_before=before,
         idx_mapping=idx_mapping, diff_rows=rows, diff_starts=starts, diff_val_offsets=offs,
-        diff_vals=vals, groups=[list(m) for m, _ in (groups or [])], seed=int(seed))
+        diff_vals=vals, groups=[list(m) for m, _ in (groups or [])],
+        group_prefix=[int(p) for _, p in (groups or [])], seed=int(seed))
 
 
 def make(cfg: int, device="cpu", kv_dtype: Optional[str] = None, sub: int = 0,
