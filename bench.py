@@ -550,8 +550,23 @@ def main():
     ap.add_argument("--requests", type=int, default=256,
                     help="decode batch size (256 is the benchmark workload; smaller sizes "
                          "are for profiling captures)")
+    ap.add_argument("--only", choices=["mixed", "long-bf16", "long-fp8", "prefix-shared", "tiny"],
+                    default=None,
+                    help="run one secondary workload alone and print its object (a narrow "
+                         "command for profiler captures; not the benchmark line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only:
+        import torch
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        run = {"mixed": lambda: run_mixed(args, dev, 3),
+               "long-bf16": lambda: run_mixed(args, dev, 5, "bf16"),
+               "long-fp8": lambda: run_mixed(args, dev, 5, "fp8"),
+               "prefix-shared": lambda: run_prefix_shared(args, dev),
+               "tiny": lambda: run_tiny(args, dev)}[args.only]
+        print(json.dumps({"only": args.only, "result": run()}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

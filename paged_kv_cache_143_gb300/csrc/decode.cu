@@ -92,11 +92,41 @@ struct SmemTail {
 };
 
 // The producer warp of both decode kernels: the warp fetches the block ids of
-// 32 chunks at a time (lane i: chunk base + i, one coalesced load); lane 0
-// issues one bulk copy of K and one of V per 16-key chunk into the ring.
+// 32 chunks at a time (lane i: chunk base + i, one coalesced load). Per 16-key
+// chunk, K and V are each one contiguous run of the pool. Runs of 4 KB and
+// more go as one bulk async copy each, issued by lane 0 (completing on the
+// stage's mbarrier by transaction bytes); smaller runs (E4M3 codes) go as
+// 16-byte asynchronous copies spread over the 32 lanes, each lane's copies
+// completing one arrival on the stage's mbarrier. The bulk-copy engine
+// completes about as many copies per second whatever their size, so small
+// runs would halve the bandwidth.
+template <class G>
+struct ProducerKind {
+  static constexpr bool kLanes = G::kChunkBytes < 4096;  // lane copies, else bulk
+  static constexpr unsigned kArrivals = kLanes ? 32u : 1u;  // full-barrier count
+};
+
+__device__ __forceinline__ void lane_copy16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+
+// One arrival on `bar` once every earlier lane_copy16 of this thread has landed.
+__device__ __forceinline__ void lane_copies_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 template <class G>
 __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
                                         int r, int kvh, int k_begin, int nch, int lane) {
+  constexpr bool kLanes = ProducerKind<G>::kLanes;
+  // chunks handled per step: lane i < kGroup waits for the stage of chunk
+  // c0 + i and (bulk copies) issues it, so the waits and the copy issue of a
+  // group overlap instead of running one chunk after another
+  constexpr int kGroup = G::kStages / 2 < 8 ? G::kStages / 2 : 8;
+  static_assert(32 % kGroup == 0, "groups must tile the 32 chunks of a block-id fetch");
   const unsigned full = 0xffffffffu;
   const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
   const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
@@ -109,36 +139,52 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
     const bool bad = c_lane < nch && (blk_lane < 0 || blk_lane >= p.num_blocks);
     if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
     if (bad) blk_lane = 0;  // read a valid block; the call's output is then unspecified
+    // byte offset of each lane's chunk in the pool (one contiguous run of K, of V)
+    const int64_t off_lane = ((int64_t)blk_lane * p.Hkv + kvh) * head_stride +
+                             (int64_t)(key_lane % p.B) * G::kRowBytes;
     const int n = min(32, nch - base);
-    for (int i = 0; i < n; ++i) {
-      const int c = base + i;
-      const int blk = __shfl_sync(full, blk_lane, i);
-      if (lane == 0) {
-        const int stage = c % G::kStages, round = c / G::kStages;
-        if (round > 0 && !mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err)) {
-          tail->abort = 1;
-          ok = false;
-        } else if (*reinterpret_cast<volatile int*>(&tail->abort)) {
-          ok = false;
-        } else {
-          const int key0 = k_begin + c * kChunk;
-          const int64_t off = ((int64_t)blk * p.Hkv + kvh) * head_stride +
-                              (int64_t)(key0 % p.B) * G::kRowBytes;
-          uint8_t* dst = ring + stage * G::kStageBytes;
-          mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
-          bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
-          bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
-          issued = c + 1;
-        }
+    for (int g0 = 0; g0 < n; g0 += kGroup) {
+      const int gn = min(kGroup, n - g0);
+      const int c = base + g0 + lane;  // this lane's chunk of the group
+      const bool mine = lane < gn;
+      const int stage = c % G::kStages, round = c / G::kStages;
+      bool free_ok = true;
+      if (mine && round > 0) free_ok = mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err);
+      ok = __all_sync(full, free_ok) && !*reinterpret_cast<volatile int*>(&tail->abort);
+      if (!ok) {
+        if (lane == 0) tail->abort = 1;
+        break;
       }
-      ok = __shfl_sync(full, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
+      const int64_t off = __shfl_sync(full, off_lane, (g0 + lane) & 31);
+      if constexpr (kLanes) {
+        // every lane copies its 16-byte pieces of each chunk of the group
+        for (int i = 0; i < gn; ++i) {
+          const int ci = base + g0 + i;
+          const int64_t oi = __shfl_sync(full, off, i);
+          uint8_t* dst = ring + (ci % G::kStages) * G::kStageBytes;
+#pragma unroll
+          for (int k = lane * 16; k < G::kChunkBytes; k += 32 * 16) {
+            lane_copy16(dst + k, p.k_pool + oi + k);
+            lane_copy16(dst + G::kChunkBytes + k, p.v_pool + oi + k);
+          }
+          lane_copies_arrive(&tail->full[ci % G::kStages]);
+        }
+      } else if (mine) {
+        uint8_t* dst = ring + stage * G::kStageBytes;
+        mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
+        bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
+        bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
+      }
+      issued = base + g0 + gn;
     }
   }
   // drain: every issued copy has landed before the CTA may exit
-  if (lane == 0)
+  if constexpr (kLanes) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (lane == 0) {
     for (int c = issued - G::kStages > 0 ? issued - G::kStages : 0; c < issued; ++c)
       mbar_wait(&tail->full[c % G::kStages], (c / G::kStages) & 1, p.err);
+  }
 }
 
 // GH heads per warp, HG head groups per CTA (GH * HG = g).
@@ -187,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->full[i], ProducerKind<G>::kArrivals);
       mbar_init(&tail->empty[i], HG);  // one arrival per head group
     }
     tail->abort = 0;
@@ -456,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->full[i], ProducerKind<G>::kArrivals);
       mbar_init(&tail->empty[i], 1);
     }
     tail->abort = 0;
@@ -715,33 +761,70 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
   }
 }
 
-// One CTA per (query head, request) with more than one split: combines the
-// partials of the decode kernel by log-sum-exp.
+// One warp per (query head, request) with more than one split slot: combines
+// the partials by log-sum-exp. Lane i holds the (max, sum) of slots i, i+32,
+// ... and dims (D/32) i .. (D/32) i + D/32 - 1 of every slot's output, so the
+// loads of all slots go out together.
+constexpr int kMergeWarps = 8;
 template <int D>
-__global__ void __launch_bounds__(D) merge_kernel(DecodeParams p) {
-  const int h = blockIdx.x, r = blockIdx.y, d = threadIdx.x;
-  const int qs = p.qsl[r];
-  if (p.qsl[r + 1] - qs != 1) return;
-  const int seq = p.seq_lens[r];
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeParams p) {
+  constexpr int kV = D / 32;  // dims per lane
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x * kMergeWarps + (threadIdx.x >> 5), r = blockIdx.y;
+  if (h >= p.Hq) return;
+  const int qs = p.qsl[r], qe = p.qsl[r + 1], seq = p.seq_lens[r];
+  if (qe - qs != 1) return;
   if (seq < 1 || seq > p.max_blocks * p.B) return;
   const int grp_id = group_of(p.groups, r);
   const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
   if (k_lo >= seq) return;
-  // slots: the shared-prefix partial (group members) and the splits
+  // slots: the shared-prefix pieces (group members) and the splits
   const int nsplit =
       prefix_slots(p.groups, grp_id) + (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
   if (nsplit <= 1 || nsplit > p.ws_splits) return;
   const int64_t row0 = ((int64_t)r * p.Hq + h) * p.ws_splits;
+  const unsigned full = 0xffffffffu;
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p.ws_ml[row0 + s].x);
-  float L = 0.f, O = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float2 ml = p.ws_ml[row0 + s];
-    const float f = exp2f(ml.x - M);
-    L += f * ml.y;
-    O += f * p.ws_o[(row0 + s) * D + d];
+  for (int s = lane; s < nsplit; s += 32) M = fmaxf(M, p.ws_ml[row0 + s].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(full, M, o));
+  float L = 0.f, O[kV];
+#pragma unroll
+  for (int v = 0; v < kV; ++v) O[v] = 0.f;
+  for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const int n = min(32, nsplit - s0);
+    float f = 0.f;
+    if (lane < n) {
+      const float2 ml = p.ws_ml[row0 + s0 + lane];
+      f = exp2f(ml.x - M);
+      L += f * ml.y;
+    }
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float fi = __shfl_sync(full, f, i);
+      const float* src = p.ws_o + (row0 + s0 + i) * D + kV * lane;
+      if constexpr (kV == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        O[0] += fi * x.x; O[1] += fi * x.y; O[2] += fi * x.z; O[3] += fi * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        O[0] += fi * x.x; O[1] += fi * x.y;
+      }
+    }
   }
-  p.out[((int64_t)qs * p.Hq + h) * D + d] = __float2bfloat16_rn(O / L);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(full, L, o);
+  __nv_bfloat16* dst = p.out + ((int64_t)qs * p.Hq + h) * D + kV * lane;
+  if constexpr (kV == 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(O[0] / L, O[1] / L);
+    __nv_bfloat162 b = __floats2bfloat162_rn(O[2] / L, O[3] / L);
+    uint2 w;
+    w.x = *reinterpret_cast<uint32_t*>(&a);
+    w.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(O[0] / L, O[1] / L);
+  }
 }
 
 template <int D, bool FP8, int GH>
@@ -795,11 +878,11 @@ cudaError_t launch_decode(const DecodeParams& p, int D, bool fp8, int R, int max
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int D, int R, cudaStream_t s) {
-  dim3 grid(p.Hq, R);
+  dim3 grid((p.Hq + kMergeWarps - 1) / kMergeWarps, R);
   if (D == 128)
-    merge_kernel<128><<<grid, 128, 0, s>>>(p);
+    merge_kernel<128><<<grid, kMergeWarps * 32, 0, s>>>(p);
   else
-    merge_kernel<64><<<grid, 64, 0, s>>>(p);
+    merge_kernel<64><<<grid, kMergeWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -70,13 +70,25 @@ struct Smem {
   static constexpr int kOffQ = 0;                      // Q_A, then Q_B
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  // E4M3 pools: one staging tile of codes for K and for V, rows of D bytes
-  static constexpr int kK8Bytes = F8 ? kN * D : 0;
+  // E4M3 pools: the tile of codes (rows of D bytes) of stage st lands in the
+  // upper half of its own f16 stage for D = 128 and is widened in place (row r
+  // of codes occupies exactly the bytes of row r of the upper 64-column chunk,
+  // so a row's codes are read before its second half is written); for D = 64
+  // each stage has a staging tile of its own.
+  static constexpr bool kInPlace = F8 && D == 128;
+  static constexpr int kK8Bytes = F8 && !kInPlace ? kN * D : 0;  // per stage
   static constexpr int kOffK8 = kOffV + kStages * kKVBytes;
-  static constexpr int kOffV8 = kOffK8 + kK8Bytes;
-  static constexpr int kOffBar = kOffV8 + kK8Bytes;
+  static constexpr int kOffV8 = kOffK8 + kStages * kK8Bytes;
+  static constexpr int kOffBar = kOffV8 + kStages * kK8Bytes;
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kAlloc = kBytes + 1024;  // the base is rounded up to 1024 B
+  static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB per-block limit");
+  __host__ __device__ static constexpr int k8(int st) {
+    return kInPlace ? kOffK + st * kKVBytes + kKVBytes / 2 : kOffK8 + st * kK8Bytes;
+  }
+  __host__ __device__ static constexpr int v8(int st) {
+    return kInPlace ? kOffV + st * kKVBytes + kKVBytes / 2 : kOffV8 + st * kK8Bytes;
+  }
 };
 
 struct Bars {
@@ -89,9 +101,8 @@ struct Bars {
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t final_mma;
-  uint64_t k8_full, v8_full;    // E4M3 staging tile landed
-  uint64_t k8_empty, v8_empty;  // E4M3 staging tile converted
-  uint64_t q_conv;              // Q tiles converted to f16 (E4M3 pools)
+  uint64_t k8_full[4], v8_full[4];  // E4M3 codes of a stage landed (k/v_full: widened)
+  uint64_t q_conv;                  // Q tiles converted to f16 (E4M3 pools)
   uint32_t tmem_base;
   int abort;
 };
@@ -197,11 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], F8 ? 2 : 1);
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->k8_full[s], 1);
+      mbar_init(&bars->v8_full[s], 1);
     }
-    mbar_init(&bars->k8_full, 1);
-    mbar_init(&bars->v8_full, 1);
-    mbar_init(&bars->k8_empty, 2);
-    mbar_init(&bars->v8_empty, 2);
     mbar_init(&bars->q_conv, 8);
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -262,16 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = (uint32_t)(nload * p.B * D * (F8 ? 1 : 2));
       const bool issues = F8 ? lane < nload : box_block < nload;
       const int row = ((F8 ? blk_lane : blk) * p.Hkv + kvh) * p.B;
-      const int dst_off =
-          F8 ? lane * p.B * D
-             : st * S::kKVBytes + box_chunk * S::kChunkBytes + box_block * p.B * 128;
-      uint64_t* kbar = F8 ? &bars->k8_full : &bars->k_full[st];
-      uint64_t* vbar = F8 ? &bars->v8_full : &bars->v_full[st];
-      // K of tile j: bf16 — its stage is free once the S MMAs of tile j - kStages
-      // are done; E4M3 — the staging tile is free once tile j - 1 is converted
+      // bf16: boxes of 64 columns into the swizzled stage; E4M3: one box of
+      // D codes x B keys per block into the stage's tile of codes
+      const int k_dst = F8 ? S::k8(st) + lane * p.B * D
+                           : S::kOffK + st * S::kKVBytes + box_chunk * S::kChunkBytes +
+                                 box_block * p.B * 128;
+      const int v_dst = F8 ? S::v8(st) + lane * p.B * D : k_dst - S::kOffK + S::kOffV;
+      uint64_t* kbar = F8 ? &bars->k8_full[st] : &bars->k_full[st];
+      uint64_t* vbar = F8 ? &bars->v8_full[st] : &bars->v_full[st];
+      // K of tile j: the stage is free once the S MMAs of tile j - kStages are
+      // done (for E4M3 this implies its codes were widened, and read, before)
       bool ok = true;
-      if (F8 && lane == 0 && j >= 1) ok = mbar_wait(&bars->k8_empty, (j - 1) & 1, p.err);
-      if (!F8 && lane == 0 && j >= kStages)
+      if (lane == 0 && j >= kStages)
         ok = mbar_wait(&bars->k_empty[st], ((j / kStages) - 1) & 1, p.err);
       if (!__shfl_sync(full, ok ? 1 : 0, 0) || aborted(bars)) {
         if (lane == 0) bars->abort = 1;
@@ -280,12 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(kbar, bytes);
       __syncwarp();
       if (issues)
-        tc::tma_load_2d(smem + (F8 ? S::kOffK8 : S::kOffK) + dst_off, &tmap_k,
-                        F8 ? 0 : box_chunk * 64, row, kbar);
+        tc::tma_load_2d(smem + k_dst, &tmap_k, F8 ? 0 : box_chunk * 64, row, kbar);
       issued_k = j + 1;
-      // V of tile j: bf16 — free once the PV MMAs of tile j - kStages are done
-      if (F8 && lane == 0 && j >= 1) ok = mbar_wait(&bars->v8_empty, (j - 1) & 1, p.err);
-      if (!F8 && lane == 0 && j >= kStages)
+      // V of tile j: free once the PV MMAs of tile j - kStages are done
+      if (lane == 0 && j >= kStages)
         ok = mbar_wait(&bars->v_empty[st], ((j / kStages) - 1) & 1, p.err);
       if (!__shfl_sync(full, ok ? 1 : 0, 0)) {
         if (lane == 0) bars->abort = 1;
@@ -294,23 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(vbar, bytes);
       __syncwarp();
       if (issues)
-        tc::tma_load_2d(smem + (F8 ? S::kOffV8 : S::kOffV) + dst_off, &tmap_v,
-                        F8 ? 0 : box_chunk * 64, row, vbar);
+        tc::tma_load_2d(smem + v_dst, &tmap_v, F8 ? 0 : box_chunk * 64, row, vbar);
       issued_v = j + 1;
       ids = next;
     }
     // every issued copy lands before the CTA may leave
     if (lane == 0) {
       mbar_wait(&bars->q_full, 0, p.err);
-      if (F8) {
-        if (issued_k > 0) mbar_wait(&bars->k8_full, (issued_k - 1) & 1, p.err);
-        if (issued_v > 0) mbar_wait(&bars->v8_full, (issued_v - 1) & 1, p.err);
-      } else {
-        for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
-          mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err);
-        for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
-          mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err);
-      }
+      for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
+        mbar_wait(F8 ? &bars->k8_full[j % kStages] : &bars->k_full[j % kStages],
+                  (j / kStages) & 1, p.err);
+      for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
+        mbar_wait(F8 ? &bars->v8_full[j % kStages] : &bars->v_full[j % kStages],
+                  (j / kStages) & 1, p.err);
     }
     } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -377,15 +382,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Each 16-byte granule of codes (16 dims of one key) becomes two 16-byte
     // f16 granules at their 128-byte-swizzled places in the K/V tile; keys at
     // or past n_kv_all are written as zeros (so P = 0 never meets a NaN).
+    // A warp covers whole key rows in each step (8 granules per row for
+    // D = 128) and reads them all before it writes any, which makes the
+    // in-place widening safe: only row r's own codes share bytes with row r's
+    // upper half.
     const int tid = threadIdx.x - 64;  // 0..63
     constexpr int kGran = D / 16;       // granules of codes per key
+    static_assert(32 % kGran == 0, "a warp step must cover whole key rows");
     auto convert = [&](const uint8_t* src, uint8_t* dst, int key0) {
 #pragma unroll 4
       for (int G = tid; G < kN * kGran; G += 64) {
         const int row = G / kGran, gq = G % kGran;
         uint32_t h[8];
-        if (key0 + row < n_kv_all) {
-          const uint4 in = *reinterpret_cast<const uint4*>(src + row * D + gq * 16);
+        const bool live = key0 + row < n_kv_all;
+        uint4 in = make_uint4(0, 0, 0, 0);
+        if (live) in = *reinterpret_cast<const uint4*>(src + row * D + gq * 16);
+        __syncwarp();
+        if (live) {
           e4m3x16_to_f16(in, h);
         } else {
 #pragma unroll
@@ -402,21 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntk_all && ok; ++j) {
       const int st = j % kStages;
       for (int kv = 0; kv < 2 && ok; ++kv) {
-        uint64_t* landed = kv ? &bars->v8_full : &bars->k8_full;
-        uint64_t* freed = kv ? &bars->v_empty[st] : &bars->k_empty[st];
-        ok = __all_sync(0xffffffffu, mbar_wait(landed, j & 1, p.err)) &&
-             (j < kStages ||
-              __all_sync(0xffffffffu, mbar_wait(freed, ((j / kStages) - 1) & 1, p.err))) &&
+        // the codes landed; the producer issued them only once the stage was
+        // free (its MMAs of tile j - kStages done)
+        uint64_t* landed = kv ? &bars->v8_full[st] : &bars->k8_full[st];
+        ok = __all_sync(0xffffffffu, mbar_wait(landed, (j / kStages) & 1, p.err)) &&
              !aborted(bars);
         if (!ok) break;
-        convert(smem + (kv ? S::kOffV8 : S::kOffK8),
+        convert(smem + (kv ? S::v8(st) : S::k8(st)),
                 smem + (kv ? S::kOffV : S::kOffK) + st * S::kKVBytes, j * kN);
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
-          mbar_arrive(kv ? &bars->v8_empty : &bars->k8_empty);
-        }
+        if (lane == 0) mbar_arrive(kv ? &bars->v_full[st] : &bars->k_full[st]);
       }
     }
     if (!ok) bars->abort = 1;
