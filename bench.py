@@ -395,14 +395,45 @@ def run_prefix_shared(args, dev):
     return res
 
 
-def run_tiny(args, dev):
-    """The tiny decode batch (4 requests): latency of one step, in microseconds."""
+def run_tiny(args, dev, graph_steps=8):
+    """The tiny decode batch (4 requests): latency of one step, in
+    microseconds, issued call by call, and the same decode steps replayed
+    `graph_steps` at a time from one CUDA graph (pa_decode_graph_*)."""
     import torch
     import workloads
+    from paged_kv_cache_143_gb300 import pa
+    stream = torch.cuda.current_stream()
     w = workloads.make(1, device=dev)
     step = Step(w, dev, max_splits=8)
-    us = timed(step.run, max(args.steps, 20), args.warmup, torch.cuda.current_stream()) * 1e3
-    return {"workload": w.name, "us_per_step": round(us, 2)}
+    us = timed(step.run, max(args.steps, 20), args.warmup, stream) * 1e3
+    # the same requests with graph_steps decode steps ahead (same shapes, seed)
+    N = graph_steps
+    ctx = [int(x) - 1 for x in w.seq_lens]
+    wg = workloads.build([c + N for c in ctx], [N] * w.R, w.Hq, w.Hkv, w.D, w.B,
+                         pool_blocks=w.num_blocks, seed=w.seed, device=dev)
+    sg = Step(wg, dev, max_splits=8)
+    pa.apply_staged_writes(sg.table, sg.rows, sg.starts, sg.offs, sg.vals, sg.idx, sg.gathered)
+    nc0 = torch.zeros(wg.max_reqs, dtype=torch.int32, device=dev)
+    nc0[sg.idx.long()] = torch.tensor(ctx, dtype=torch.int32, device=dev)
+    nc = nc0.clone()
+    per_step = lambda t: t.view(wg.R, N, *t.shape[1:]).transpose(0, 1).contiguous()
+    q, k, v = per_step(sg.q), per_step(sg.new_k), per_step(sg.new_v)
+    out = torch.empty_like(q)
+    g = pa.DecodeGraph(sg.pool, wg.scale, nc, sg.table, sg.idx, sg.gathered,
+                       [c + N for c in ctx], q, k, v, out, workspace=sg.ws)
+
+    def replay():
+        nc.copy_(nc0)  # every launch starts from the same slot state
+        g.launch()
+    us_graph = timed(replay, max(args.steps, 20), args.warmup, stream) * 1e3 / N
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the tiny decode runs")
+    kernels = g.kernels
+    g.close()
+    return {"workload": w.name, "us_per_step": round(us, 2),
+            "graph": {"steps_per_launch": N, "us_per_step": round(us_graph, 2),
+                      "kernels_per_launch": kernels,
+                      "step": "pa_prepare_inputs + pa_write_kv + pa_forward, captured"}}
 
 
 def load_peaks_tensor():

@@ -211,6 +211,110 @@ pa_status pa_forward_shared_prefix(const void* q, void* out, const int32_t* quer
                                    size_t workspace_bytes, pa_stream_t stream);
 
 /*
+ * pa_prepare_inputs — one step's attention inputs built on the device from
+ * per-slot state, so that the host sends only (slot, token count) per request
+ * and the block-table diffs.
+ * [MRV2, "재설계 1"]: a live request keeps a fixed persistent slot; entry i of
+ * the step is slot idx_mapping[i]. [MRV2, "재설계 4"]: query_start_loc,
+ * positions, seq_lens and the slot mapping are prepared on the GPU.
+ * [vLLM-wiki, "블록 테이블"]: position p lives in logical block p / B at offset
+ * p % B; its pool slot is physical_block * B + offset.
+ *
+ *   num_computed     dev int32 [max_reqs]: tokens of each slot whose K/V are
+ *                    stored; read, then advanced by the step's counts
+ *   table            dev int32 [max_reqs][max_blocks]: the persistent block
+ *                    table (after pa_apply_staged_writes)
+ *   idx_mapping      dev int32 [R]: slot of entry i (each slot at most once)
+ *   num_scheduled    dev int32 [R]: tokens of entry i this step (>= 0);
+ *                    NULL: one token per entry (a decode step)
+ *   token_capacity   entries of positions / slot_mapping
+ *   query_start_loc  dev int32 [R+1]  out: running sum of num_scheduled
+ *   seq_lens         dev int32 [R]    out: num_computed[slot] + num_scheduled
+ *   positions        dev int32 [T]    out: the tokens' positions
+ *   slot_mapping     dev int64 [T]    out: the tokens' pool slots (input of
+ *                                     pa_write_kv)
+ *
+ * One launch on `stream`. Integer work: exactly the definition above. A slot
+ * outside [0, max_reqs), a negative count, a total above token_capacity, a
+ * position past the table row or a block outside [0, num_blocks) sets
+ * PA_ERR_DEVICE_BOUNDS (read by pa_get_error); such slots are written as -1
+ * (pa_write_kv skips them) and nothing is written outside the buffers. A slot
+ * listed twice gives unspecified counts. Host checks: PA_ERR_INVALID for
+ * negative sizes or NULL buffers that the sizes require.
+ */
+pa_status pa_prepare_inputs(int32_t* num_computed, int32_t max_reqs, const int32_t* table,
+                            int32_t max_blocks, int32_t block_size, int32_t num_blocks,
+                            const int32_t* idx_mapping, const int32_t* num_scheduled,
+                            int32_t num_reqs, int32_t token_capacity, int32_t* query_start_loc,
+                            int32_t* seq_lens, int32_t* positions, int64_t* slot_mapping,
+                            pa_stream_t stream);
+
+/*
+ * pa_decode_graph_* — several decode steps of the same requests captured once
+ * into a CUDA graph and replayed with one launch.
+ * [V1-blog, "PagedAttention V3 커널 아키텍처와 하드웨어 레벨 메모리 정렬",
+ * multi-step scheduling bullet]: N decode steps (4 to 8, say) run from a CUDA
+ * graph without a host round trip per token. [MRV2, "재설계 4"]: graphs are
+ * managed explicitly; each captured shape costs capture time and memory.
+ *
+ * Step s of the graph (s = 0 .. num_steps-1) is exactly this eager sequence:
+ *   pa_prepare_inputs(num_computed, ..., idx_mapping, NULL (one token each),
+ *                     num_reqs, num_reqs, query_start_loc, seq_lens, positions,
+ *                     slot_mapping)
+ *   pa_write_kv(pool, k_new + s * R*Hkv*D, v_new + s * R*Hkv*D, slot_mapping, R)
+ *   pa_forward(q + s * R*Hq*D, out + s * R*Hq*D, query_start_loc, seq_lens,
+ *              {0, 1, .., R}, seq_len_bound_host, block_tables, max_blocks, R, R,
+ *              num_q_heads, pool, scale, 1, workspace, workspace_bytes)
+ * so every output equals that of the eager calls made with the same bound.
+ * The forward plan is fixed at creation from seq_len_bound_host; every launch
+ * must keep each request's sequence length (num_computed + 1 at each step) at
+ * or below its bound, else the kernels set PA_ERR_DEVICE_BOUNDS (no read out
+ * of range). The table must already hold the blocks of every position the
+ * steps write; block_tables holds the rows table[idx_mapping[i]].
+ *
+ * The pool struct, pointers and sizes are read at creation and baked into the
+ * graph: the buffers must stay allocated and in place until destroy. The
+ * graph object is created (host and driver memory) by create and released by
+ * destroy; the library allocates no device memory. Launches of one graph must
+ * not overlap (they share the scratch buffers); launch returns without
+ * waiting. Errors: PA_ERR_INVALID (NULL or non-positive sizes), the status of
+ * the first captured call that fails, PA_ERR_CUDA if capture or instantiation
+ * fails.
+ */
+typedef struct pa_decode_graph pa_decode_graph;
+
+typedef struct {
+  const pa_kv_pool* pool;
+  float scale;
+  int32_t num_q_heads;
+  int32_t num_reqs;                    /* R: decode requests, one token per step  */
+  int32_t num_steps;                   /* N                                        */
+  int32_t* num_computed;               /* dev int32 [max_reqs] (advanced N / launch) */
+  int32_t max_reqs;
+  const int32_t* table;                /* dev int32 [max_reqs][max_blocks]         */
+  int32_t max_blocks;
+  const int32_t* idx_mapping;          /* dev int32 [R]                            */
+  const int32_t* block_tables;         /* dev int32 [R][max_blocks]                */
+  const int32_t* seq_len_bound_host;   /* host int32 [R]                           */
+  const void* q;                       /* dev bf16 [N][R][Hq][D]                   */
+  const void* k_new;                   /* dev bf16 [N][R][Hkv][D]                  */
+  const void* v_new;                   /* dev bf16 [N][R][Hkv][D]                  */
+  void* out;                           /* dev bf16 [N][R][Hq][D]                   */
+  int32_t* query_start_loc;            /* dev scratch int32 [R+1]                  */
+  int32_t* seq_lens;                   /* dev scratch int32 [R]                    */
+  int32_t* positions;                  /* dev scratch int32 [R]                    */
+  int64_t* slot_mapping;               /* dev scratch int64 [R]                    */
+  void* workspace;                     /* as pa_forward (may be NULL / 0)          */
+  size_t workspace_bytes;
+} pa_decode_graph_desc;
+
+pa_status pa_decode_graph_create(const pa_decode_graph_desc* desc, pa_decode_graph** graph);
+pa_status pa_decode_graph_launch(pa_decode_graph* graph, pa_stream_t stream);
+void pa_decode_graph_destroy(pa_decode_graph* graph);
+/* Kernel launches one pa_decode_graph_launch performs (0 for NULL). */
+uint32_t pa_decode_graph_kernels(const pa_decode_graph* graph);
+
+/*
  * pa_apply_staged_writes — apply packed block-table diffs, then gather the
  * rows of this step.
  * [MRV2, "재설계 3: 큰 block table은 staged diff만 보낸다"]: the device copy of the

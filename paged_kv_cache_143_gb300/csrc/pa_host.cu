@@ -49,6 +49,8 @@ int num_sms() {
 }
 
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+void uncount_launches(unsigned n) { g_launches.fetch_sub(n, std::memory_order_relaxed); }
+unsigned long long launches_so_far() { return g_launches.load(std::memory_order_relaxed); }
 
 pa_status check_pool(const pa_kv_pool* pool) {
   if (!pool || !pool->k_pool || !pool->v_pool) return PA_ERR_INVALID;

@@ -22,6 +22,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Counts `n` kernel launches made by the library (reported by
 // pa_kernel_launches).
 void count_launches(unsigned n);
+// Takes back launches counted while a stream was being captured (they run
+// when the graph is launched), and reads the running count.
+void uncount_launches(unsigned n);
+unsigned long long launches_so_far();
 
 // Maps the result of a launch (cudaGetLastError after <<<>>>) to a status and
 // counts the launch when it succeeded.

@@ -24,7 +24,9 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
            "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
-           "pa_forward_noalloc", "pa_selftest_wait_timeout", "pa_forward_shared_prefix")
+           "pa_forward_noalloc", "pa_selftest_wait_timeout", "pa_forward_shared_prefix",
+           "pa_prepare_inputs", "pa_decode_graph_create", "pa_decode_graph_launch",
+           "pa_decode_graph_destroy", "pa_decode_graph_kernels")
 
 
 class PaError(RuntimeError):
@@ -39,6 +41,20 @@ class _Pool(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("dtype", ctypes.c_int32), ("k_scale", ctypes.c_float),
                 ("v_scale", ctypes.c_float)]
+
+
+class _DecodeGraphDesc(ctypes.Structure):
+    _fields_ = [("pool", ctypes.POINTER(_Pool)), ("scale", ctypes.c_float),
+                ("num_q_heads", ctypes.c_int32), ("num_reqs", ctypes.c_int32),
+                ("num_steps", ctypes.c_int32), ("num_computed", ctypes.c_void_p),
+                ("max_reqs", ctypes.c_int32), ("table", ctypes.c_void_p),
+                ("max_blocks", ctypes.c_int32), ("idx_mapping", ctypes.c_void_p),
+                ("block_tables", ctypes.c_void_p), ("seq_len_bound_host", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("query_start_loc", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+                ("slot_mapping", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -75,6 +91,17 @@ def lib():
         L.pa_forward_shared_prefix.restype = ctypes.c_int
         L.pa_forward_shared_prefix.argtypes = [P, P, P, P, P, P, P, I32, I32, I32, I32, PP, F32,
                                                I32, I32, P, P, P, P, SZ, P]
+        L.pa_prepare_inputs.restype = ctypes.c_int
+        L.pa_prepare_inputs.argtypes = [P, I32, P, I32, I32, I32, P, P, I32, I32, P, P, P, P, P]
+        L.pa_decode_graph_create.restype = ctypes.c_int
+        L.pa_decode_graph_create.argtypes = [ctypes.POINTER(_DecodeGraphDesc),
+                                             ctypes.POINTER(ctypes.c_void_p)]
+        L.pa_decode_graph_launch.restype = ctypes.c_int
+        L.pa_decode_graph_launch.argtypes = [P, P]
+        L.pa_decode_graph_destroy.restype = None
+        L.pa_decode_graph_destroy.argtypes = [P]
+        L.pa_decode_graph_kernels.restype = ctypes.c_uint32
+        L.pa_decode_graph_kernels.argtypes = [P]
         L.pa_selftest_wait_timeout.restype = ctypes.c_int
         L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_kernel_launches.restype = ctypes.c_uint64
@@ -240,6 +267,90 @@ def forward_noalloc(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.T
         Hq, ctypes.byref(pool.struct()), float(scale), int(causal), int(max_splits),
         _stream(stream))
     _check(st, "pa_forward_noalloc")
+
+
+def prepare_inputs(num_computed: torch.Tensor, table: torch.Tensor, block_size: int,
+                   num_blocks: int, idx_mapping: torch.Tensor, num_scheduled: torch.Tensor,
+                   query_start_loc: torch.Tensor, seq_lens: torch.Tensor,
+                   positions: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """Device-side step inputs from per-slot state (pa_prepare_inputs); the
+    outputs are written into the given device tensors."""
+    max_reqs, max_blocks = table.shape
+    R = idx_mapping.numel()
+    st = lib().pa_prepare_inputs(
+        _dptr(num_computed, torch.int32), max_reqs, _dptr(table, torch.int32), max_blocks,
+        int(block_size), int(num_blocks), _dptr(idx_mapping, torch.int32),
+        _dptr(num_scheduled, torch.int32), R, positions.numel(),
+        _dptr(query_start_loc, torch.int32), _dptr(seq_lens, torch.int32),
+        _dptr(positions, torch.int32), _dptr(slot_mapping, torch.int64), _stream(stream))
+    _check(st, "pa_prepare_inputs")
+
+
+class DecodeGraph:
+    """pa_decode_graph_*: `num_steps` decode steps of the same requests
+    captured once into a CUDA graph (prepare inputs, write K/V, attention per
+    step) and replayed by launch(). Every tensor passed here must stay alive
+    and in place while the graph exists; this object keeps references to
+    them. The plan is fixed from seq_len_bound (host, per request)."""
+
+    def __init__(self, pool: KVPool, scale: float, num_computed: torch.Tensor,
+                 table: torch.Tensor, idx_mapping: torch.Tensor, block_tables: torch.Tensor,
+                 seq_len_bound, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                 out: torch.Tensor, workspace: Optional[torch.Tensor] = None):
+        N, R, Hq, D = q.shape
+        self._bound = _host_i32(seq_len_bound)
+        dev = q.device
+        self.query_start_loc = torch.empty(R + 1, dtype=torch.int32, device=dev)
+        self.seq_lens = torch.empty(R, dtype=torch.int32, device=dev)
+        self.positions = torch.empty(R, dtype=torch.int32, device=dev)
+        self.slot_mapping = torch.empty(R, dtype=torch.int64, device=dev)
+        self._pool_struct = pool.struct()
+        self._keep = (pool, num_computed, table, idx_mapping, block_tables, q, k_new, v_new, out,
+                      workspace)
+        d = _DecodeGraphDesc()
+        d.pool = ctypes.pointer(self._pool_struct)
+        d.scale = float(scale)
+        d.num_q_heads, d.num_reqs, d.num_steps = Hq, R, N
+        d.num_computed = _dptr(num_computed, torch.int32)
+        d.max_reqs = table.shape[0]
+        d.table = _dptr(table, torch.int32)
+        d.max_blocks = table.shape[1]
+        d.idx_mapping = _dptr(idx_mapping, torch.int32)
+        d.block_tables = _dptr(block_tables, torch.int32)
+        d.seq_len_bound_host = self._bound.ctypes.data_as(ctypes.c_void_p)
+        d.q = _dptr(q, torch.bfloat16)
+        d.k_new = _dptr(k_new, torch.bfloat16)
+        d.v_new = _dptr(v_new, torch.bfloat16)
+        d.out = _dptr(out, torch.bfloat16)
+        d.query_start_loc = _dptr(self.query_start_loc)
+        d.seq_lens = _dptr(self.seq_lens)
+        d.positions = _dptr(self.positions)
+        d.slot_mapping = _dptr(self.slot_mapping)
+        d.workspace = _dptr(workspace) if workspace is not None else None
+        d.workspace_bytes = workspace.numel() if workspace is not None else 0
+        self._desc = d
+        h = ctypes.c_void_p()
+        _check(lib().pa_decode_graph_create(ctypes.byref(d), ctypes.byref(h)),
+               "pa_decode_graph_create")
+        self._h = h
+
+    @property
+    def kernels(self) -> int:
+        return int(lib().pa_decode_graph_kernels(self._h))
+
+    def launch(self, stream=None) -> None:
+        _check(lib().pa_decode_graph_launch(self._h, _stream(stream)), "pa_decode_graph_launch")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().pa_decode_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def apply_staged_writes(table: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,
