@@ -24,12 +24,14 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    """CUDA translation units and host-only C++ ones (the scheduler)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(
-        os.path.join(CSRC, "*.cuh")) + [os.path.join(os.path.dirname(HERE), "include", "pa.h")]
+        os.path.join(CSRC, "*.cuh")) + glob.glob(
+        os.path.join(os.path.dirname(HERE), "include", "*.h"))
 
 
 def up_to_date() -> bool:

@@ -26,7 +26,11 @@ EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_s
            "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
            "pa_forward_noalloc", "pa_selftest_wait_timeout", "pa_forward_shared_prefix",
            "pa_prepare_inputs", "pa_decode_graph_create", "pa_decode_graph_launch",
-           "pa_decode_graph_destroy", "pa_decode_graph_kernels")
+           "pa_decode_graph_destroy", "pa_decode_graph_kernels",
+           # include/pa_sched.h
+           "pa_sched_create", "pa_sched_destroy", "pa_sched_add_request", "pa_sched_fork",
+           "pa_sched_abort", "pa_sched_step", "pa_sched_commit", "pa_sched_get_stats",
+           "pa_sched_block_table")
 
 
 class PaError(RuntimeError):
@@ -55,6 +59,34 @@ class _DecodeGraphDesc(ctypes.Structure):
                 ("seq_lens", ctypes.c_void_p), ("positions", ctypes.c_void_p),
                 ("slot_mapping", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_size_t)]
+
+
+I32P, I64P = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+
+
+class _SchedConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_blocks", "block_size", "max_reqs",
+                                                "max_blocks_per_req", "token_budget",
+                                                "chunk_cap", "prefix_caching")]
+
+
+class _SchedBatch(ctypes.Structure):
+    _fields_ = [("num_reqs", ctypes.c_int32), ("num_tokens", ctypes.c_int32),
+                ("num_decode", ctypes.c_int32), ("req_ids", I64P), ("idx_mapping", I32P),
+                ("num_scheduled", I32P), ("query_start_loc", I32P), ("seq_lens", I32P),
+                ("positions", I32P), ("token_ids", I32P), ("slot_mapping", I64P),
+                ("num_diffs", ctypes.c_int32), ("diff_rows", I32P), ("diff_starts", I32P),
+                ("diff_val_offsets", I32P), ("diff_vals", I32P), ("num_copies", ctypes.c_int32),
+                ("copy_src", I32P), ("copy_dst", I32P)]
+
+
+class _SchedStats(ctypes.Structure):
+    _fields_ = [("steps", ctypes.c_int64), ("scheduled_tokens", ctypes.c_int64),
+                ("preemptions", ctypes.c_int64), ("prefix_hit_tokens", ctypes.c_int64),
+                ("finished", ctypes.c_int64), ("running", ctypes.c_int32),
+                ("waiting", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+                ("cached_free_blocks", ctypes.c_int32), ("used_blocks", ctypes.c_int32),
+                ("stored_tokens", ctypes.c_int64), ("wasted_slots", ctypes.c_int64)]
 
 
 _lib = None
@@ -102,6 +134,25 @@ def lib():
         L.pa_decode_graph_destroy.argtypes = [P]
         L.pa_decode_graph_kernels.restype = ctypes.c_uint32
         L.pa_decode_graph_kernels.argtypes = [P]
+        SP = ctypes.c_void_p
+        L.pa_sched_create.restype = ctypes.c_int
+        L.pa_sched_create.argtypes = [ctypes.POINTER(_SchedConfig), ctypes.POINTER(SP)]
+        L.pa_sched_destroy.restype = None
+        L.pa_sched_destroy.argtypes = [SP]
+        L.pa_sched_add_request.restype = ctypes.c_int
+        L.pa_sched_add_request.argtypes = [SP, I64, P, I32, I32, ctypes.c_uint64]
+        L.pa_sched_fork.restype = ctypes.c_int
+        L.pa_sched_fork.argtypes = [SP, I64, I64, I32]
+        L.pa_sched_abort.restype = ctypes.c_int
+        L.pa_sched_abort.argtypes = [SP, I64]
+        L.pa_sched_step.restype = ctypes.c_int
+        L.pa_sched_step.argtypes = [SP, ctypes.POINTER(_SchedBatch)]
+        L.pa_sched_commit.restype = ctypes.c_int
+        L.pa_sched_commit.argtypes = [SP, P, I32, P, I32, ctypes.POINTER(ctypes.c_int32)]
+        L.pa_sched_get_stats.restype = ctypes.c_int
+        L.pa_sched_get_stats.argtypes = [SP, ctypes.POINTER(_SchedStats)]
+        L.pa_sched_block_table.restype = ctypes.c_int
+        L.pa_sched_block_table.argtypes = [SP, I64, P, I32, ctypes.POINTER(ctypes.c_int32)]
         L.pa_selftest_wait_timeout.restype = ctypes.c_int
         L.pa_selftest_wait_timeout.argtypes = [P]
         L.pa_kernel_launches.restype = ctypes.c_uint64
@@ -344,6 +395,102 @@ class DecodeGraph:
     def close(self) -> None:
         if getattr(self, "_h", None):
             lib().pa_decode_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class SchedBatch:
+    """One scheduled step (numpy copies of the scheduler's arrays)."""
+    FIELDS = ("req_ids", "idx_mapping", "num_scheduled", "query_start_loc", "seq_lens",
+              "positions", "token_ids", "slot_mapping", "diff_rows", "diff_starts",
+              "diff_val_offsets", "diff_vals", "copy_src", "copy_dst")
+
+    def __init__(self, b: "_SchedBatch"):
+        R, T, W, C = b.num_reqs, b.num_tokens, b.num_diffs, b.num_copies
+        n_vals = b.diff_val_offsets[W] if W >= 0 else 0
+        sizes = dict(req_ids=R, idx_mapping=R, num_scheduled=R, query_start_loc=R + 1,
+                     seq_lens=R, positions=T, token_ids=T, slot_mapping=T, diff_rows=W,
+                     diff_starts=W, diff_val_offsets=W + 1, diff_vals=n_vals, copy_src=C,
+                     copy_dst=C)
+        for name in self.FIELDS:
+            ptr, n = getattr(b, name), sizes[name]
+            dt = np.int64 if name in ("req_ids", "slot_mapping") else np.int32
+            setattr(self, name, np.ctypeslib.as_array(ptr, shape=(n,)).astype(dt, copy=True)
+                    if n > 0 else np.zeros(0, dt))
+        self.num_decode = b.num_decode
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.req_ids.size)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1])
+
+
+class Scheduler:
+    """pa_sched_*: the native host scheduler and block manager."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_reqs: int,
+                 max_blocks_per_req: int, token_budget: int, chunk_cap: int = 1024,
+                 prefix_caching: bool = False):
+        cfg = _SchedConfig(num_blocks, block_size, max_reqs, max_blocks_per_req, token_budget,
+                           chunk_cap, 1 if prefix_caching else 0)
+        h = ctypes.c_void_p()
+        _check(lib().pa_sched_create(ctypes.byref(cfg), ctypes.byref(h)), "pa_sched_create")
+        self._h = h
+        self.block_size = block_size
+
+    def add_request(self, req_id: int, prompt, max_new: int, salt: int = 0) -> None:
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        _check(lib().pa_sched_add_request(self._h, int(req_id), p.ctypes.data_as(ctypes.c_void_p),
+                                          p.size, int(max_new), int(salt) & (2**64 - 1)),
+               "pa_sched_add_request")
+
+    def fork(self, parent: int, child: int, max_new: int) -> None:
+        _check(lib().pa_sched_fork(self._h, int(parent), int(child), int(max_new)),
+               "pa_sched_fork")
+
+    def abort(self, req_id: int) -> None:
+        _check(lib().pa_sched_abort(self._h, int(req_id)), "pa_sched_abort")
+
+    def step(self) -> SchedBatch:
+        b = _SchedBatch()
+        _check(lib().pa_sched_step(self._h, ctypes.byref(b)), "pa_sched_step")
+        return SchedBatch(b)
+
+    def commit(self, sampled):
+        s = np.ascontiguousarray(sampled, dtype=np.int32)
+        ids = np.zeros(max(s.size, 1), np.int64)
+        n = ctypes.c_int32()
+        _check(lib().pa_sched_commit(self._h, s.ctypes.data_as(ctypes.c_void_p), s.size,
+                                     ids.ctypes.data_as(ctypes.c_void_p), ids.size,
+                                     ctypes.byref(n)), "pa_sched_commit")
+        return ids[:n.value].tolist()
+
+    def stats(self) -> dict:
+        st = _SchedStats()
+        _check(lib().pa_sched_get_stats(self._h, ctypes.byref(st)), "pa_sched_get_stats")
+        return {name: getattr(st, name) for name, _ in _SchedStats._fields_}
+
+    def table(self, req_id: int):
+        n = ctypes.c_int32()
+        _check(lib().pa_sched_block_table(self._h, int(req_id), None, 0, ctypes.byref(n)),
+               "pa_sched_block_table")
+        out = np.zeros(max(n.value, 1), np.int32)
+        _check(lib().pa_sched_block_table(self._h, int(req_id),
+                                          out.ctypes.data_as(ctypes.c_void_p), out.size,
+                                          ctypes.byref(n)), "pa_sched_block_table")
+        return out[:n.value].tolist()
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().pa_sched_destroy(self._h)
             self._h = None
 
     def __del__(self):

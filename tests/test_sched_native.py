@@ -1,0 +1,106 @@
+"""The native scheduler (pa_sched_*, host C++) against the reference scheduler,
+step by step on random request streams: every batch field, every finished
+list, every live table and the block statistics must be identical. Runs on
+the CPU (the scheduler never touches the GPU)."""
+import numpy as np
+import pytest
+
+from oracle.scheduler import SchedError, Scheduler as RefScheduler
+from paged_kv_cache_143_gb300 import pa
+
+CONFIGS = [
+    # num_blocks, B, max_reqs, max_blocks, budget, cap, prefix caching
+    (512, 16, 32, 64, 256, 64, False),
+    (64, 16, 16, 48, 512, 128, False),      # tight pool: preemption
+    (256, 16, 24, 64, 300, 96, True),       # prefix reuse + LRU
+    (48, 32, 8, 24, 1024, 1024, True),      # tight pool with caching
+    (2048, 64, 64, 32, 4096, 2048, True),   # large blocks, large budget
+]
+
+
+def _compare(b_ref, b_nat):
+    for name in pa.SchedBatch.FIELDS:
+        ref = np.asarray(getattr(b_ref, name), dtype=np.int64)
+        nat = getattr(b_nat, name).astype(np.int64)
+        assert ref.tolist() == nat.tolist(), name
+    assert b_ref.num_decode == b_nat.num_decode
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=[f"c{i}" for i in range(len(CONFIGS))])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_native_matches_reference(cfg, seed):
+    nb, B, mr, mb, budget, cap, caching = cfg
+    rng = np.random.default_rng(seed * 100 + nb)
+    ref = RefScheduler(nb, B, mr, mb, budget, cap, caching)
+    nat = pa.Scheduler(nb, B, mr, mb, budget, cap, caching)
+    common = [rng.integers(0, 30000, size=int(n)).tolist() for n in (3 * B, 5 * B + 3)]
+    rid = 0
+    for step in range(250):
+        # arrivals, some sharing a prefix (and a salt that splits them)
+        for _ in range(int(rng.poisson(0.7))):
+            n = int(rng.integers(1, min(mb * B // 2, 400)))
+            prompt = rng.integers(0, 30000, size=n).tolist()
+            if rng.random() < 0.4:
+                prompt = common[int(rng.integers(0, 2))] + prompt
+            prompt = prompt[:mb * B - 40]
+            max_new = int(rng.integers(1, 40))
+            salt = int(rng.integers(0, 2)) if rng.random() < 0.3 else 0
+            ref.add_request(rid, prompt, max_new, salt)
+            nat.add_request(rid, prompt, max_new, salt)
+            rid += 1
+        if rng.random() < 0.08 and ref.running:
+            par = ref.running[int(rng.integers(0, len(ref.running)))].rid
+            try:
+                ref.fork(par, rid, int(rng.integers(1, 20)))
+                ok = True
+            except SchedError:
+                ok = False
+            if ok:
+                nat.fork(par, rid, ref.reqs[rid].max_new)
+            else:
+                with pytest.raises(pa.PaError):
+                    nat.fork(par, rid, 5)
+            rid += 1
+        if rng.random() < 0.05 and ref.reqs:
+            victim = int(rng.choice(sorted(ref.reqs)))
+            ref.abort(victim)
+            nat.abort(victim)
+        b_ref, b_nat = ref.step(), nat.step()
+        _compare(b_ref, b_nat)
+        sampled = rng.integers(0, 30000, size=len(b_ref.req_ids)).tolist()
+        assert ref.commit(sampled) == nat.commit(sampled)
+        ref.check()
+        st = nat.stats()
+        used, stored = ref.block_usage()
+        assert (st["used_blocks"], st["stored_tokens"]) == (used, stored)
+        assert st["wasted_slots"] == used * B - stored
+        assert (st["preemptions"], st["prefix_hit_tokens"], st["finished"]) == (
+            ref.stats["preemptions"], ref.stats["prefix_hit_tokens"], ref.stats["finished"])
+        assert (st["running"], st["waiting"]) == (len(ref.running), len(ref.waiting))
+        assert (st["free_blocks"], st["cached_free_blocks"]) == (len(ref.free), len(ref.lru))
+        for r in list(ref.reqs)[:8]:
+            assert nat.table(r) == ref.table(r)
+    nat.close()
+
+
+def test_native_rejects_bad_calls():
+    s = pa.Scheduler(16, 16, 2, 4, 64)
+    with pytest.raises(pa.PaError):
+        s.add_request(0, [], 1)
+    with pytest.raises(pa.PaError):
+        s.add_request(0, [1] * 60, 5)     # longer than a 4-block row
+    s.add_request(0, [1, 2], 1)
+    with pytest.raises(pa.PaError):
+        s.add_request(0, [1], 1)           # live id
+    s.step()
+    with pytest.raises(pa.PaError):
+        s.step()                           # commit first
+    with pytest.raises(pa.PaError):
+        s.commit([1, 2])                   # wrong length
+    assert s.commit([9]) == [0]
+    with pytest.raises(pa.PaError):
+        s.abort(0)                         # finished
+    with pytest.raises(pa.PaError):
+        s.fork(5, 6, 1)                    # unknown parent
+    with pytest.raises(pa.PaError):
+        pa.Scheduler(0, 16, 2, 4, 64)
