@@ -266,6 +266,7 @@ def run_libpa(args):
                             "fp8": run_mixed(args, dev, 5, "fp8")}
     line["prefix_shared"] = run_prefix_shared(args, dev)
     line["tiny_decode"] = run_tiny(args, dev)
+    line["serving"] = run_serving(args, dev)
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(line), flush=True)
@@ -436,6 +437,84 @@ def run_tiny(args, dev, graph_steps=8):
                       "step": "pa_prepare_inputs + pa_write_kv + pa_forward, captured"}}
 
 
+def run_serving(args, dev, steps=30):
+    """Multi-step serving loop (native scheduler + device calls, engine.py)
+    on a stream shaped like the mixed chunked-prefill step: 64 long-running
+    requests (prompts U[1024, 4096]) decoding while prompts of U[1024, 8192]
+    tokens arrive, 32/8 heads, head_dim 128, block 16, budget 4096 tokens,
+    chunk cap 2048. Whole-loop tokens/s (host scheduling, one pinned upload,
+    the device calls and the read-back of each entry's last output row, per
+    step), KV waste and preemptions from the scheduler's block statistics."""
+    import time
+    import torch
+    from paged_kv_cache_143_gb300 import pa
+    from paged_kv_cache_143_gb300.engine import Engine
+    Hq, Hkv, D, B, NB = 32, 8, 128, 16, 40000
+    max_reqs, max_blocks, max_tokens = 256, 1024, 4096
+    rng = np.random.default_rng(143300)
+    k_pool = torch.zeros((NB, Hkv, B, D), dtype=torch.bfloat16, device=dev)
+    v_pool = torch.zeros_like(k_pool)
+    pool = pa.KVPool(k_pool, v_pool)
+    sched = pa.Scheduler(NB, B, max_reqs, max_blocks, token_budget=4096, chunk_cap=2048)
+    eng = Engine(sched, pool, Hq, max_reqs, max_blocks, max_tokens, scale=D ** -0.5,
+                 device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(143300)
+    q = torch.randn((max_tokens, Hq, D), generator=gen, device=dev).bfloat16()
+    k = torch.randn((max_tokens, Hkv, D), generator=gen, device=dev).bfloat16()
+    v = torch.randn((max_tokens, Hkv, D), generator=gen, device=dev).bfloat16()
+    out = torch.empty_like(q)
+    rid = 0
+    for _ in range(64):
+        sched.add_request(rid, rng.integers(0, 32000, size=int(rng.integers(1024, 4097))), 4000)
+        rid += 1
+
+    def one_step():
+        nonlocal rid
+        if rng.random() < 0.35:
+            sched.add_request(rid, rng.integers(0, 32000, size=int(rng.integers(1024, 8193))),
+                              int(rng.integers(16, 256)))
+            rid += 1
+        b = eng.step(q, k, v, out)
+        eng.sync()
+        sched.commit(rng.integers(0, 32000, size=b.num_reqs))
+        return b
+    # warm-up: until the 64 long requests decode
+    for _ in range(200):
+        if one_step().num_decode >= 64:
+            break
+    for _ in range(3):
+        one_step()
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the serving warm-up")
+    st0 = sched.stats()
+    h2d0, d2h0 = eng.h2d_bytes, eng.d2h_bytes
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    toks = dec = 0
+    for _ in range(steps):
+        b = one_step()
+        toks += b.num_tokens
+        dec += b.num_decode
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the serving loop")
+    st = sched.stats()
+    used_slots = st["used_blocks"] * B
+    return {"workload": "serving loop, mixed-chunked-prefill-like stream",
+            "steps": steps, "tokens_per_s": round(toks / dt, 1),
+            "ms_per_step": round(dt * 1e3 / steps, 4),
+            "tokens_per_step": round(toks / steps, 1), "decodes_per_step": round(dec / steps, 1),
+            "h2d_bytes_per_step": int((eng.h2d_bytes - h2d0) / steps),
+            "d2h_bytes_per_step": int((eng.d2h_bytes - d2h0) / steps),
+            "kv_waste_frac": round(st["wasted_slots"] / max(used_slots, 1), 5),
+            "kv_used_blocks": st["used_blocks"], "preemptions": st["preemptions"] -
+            st0["preemptions"],
+            "step": "pa_sched_step + one pinned upload + pa_apply_staged_writes x2 + "
+                    "pa_copy_blocks + pa_prepare_inputs + pa_write_kv + pa_forward + read-back"}
+
+
 def load_peaks_tensor():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -581,7 +660,8 @@ def main():
     ap.add_argument("--requests", type=int, default=256,
                     help="decode batch size (256 is the benchmark workload; smaller sizes "
                          "are for profiling captures)")
-    ap.add_argument("--only", choices=["mixed", "long-bf16", "long-fp8", "prefix-shared", "tiny"],
+    ap.add_argument("--only", choices=["mixed", "long-bf16", "long-fp8", "prefix-shared", "tiny",
+                                       "serving"],
                     default=None,
                     help="run one secondary workload alone and print its object (a narrow "
                          "command for profiler captures; not the benchmark line)")
@@ -595,7 +675,8 @@ def main():
                "long-bf16": lambda: run_mixed(args, dev, 5, "bf16"),
                "long-fp8": lambda: run_mixed(args, dev, 5, "fp8"),
                "prefix-shared": lambda: run_prefix_shared(args, dev),
-               "tiny": lambda: run_tiny(args, dev)}[args.only]
+               "tiny": lambda: run_tiny(args, dev),
+               "serving": lambda: run_serving(args, dev)}[args.only]
         print(json.dumps({"only": args.only, "result": run()}), flush=True)
         return
     if args.impl == "reference":
