@@ -584,7 +584,7 @@ def run_e2e(args, w, step, dev, kv_bytes, world):
 # ------------------------------------------------------------- oracle arms
 
 SAMPLE_REQUESTS = 64
-BASELINE_SECONDS = 10.0
+CPU_SAMPLE_SECONDS = 10.0
 
 
 def oracle_sample_step(w):
@@ -610,7 +610,7 @@ def cpu_baseline(args, n_req=SAMPLE_REQUESTS):
     w = workloads.make(CONFIG_ID, device="cpu", sub=9, num_requests=n_req)
     kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
     secs = []
-    while not secs or sum(secs) < BASELINE_SECONDS:
+    while not secs or sum(secs) < CPU_SAMPLE_SECONDS:
         secs.append(oracle_sample_step(w))
     s = sum(secs) / len(secs)
     return {"value": round(kv / s / 1e9, 4), "unit": UNIT, "cores": O.max_threads(),
