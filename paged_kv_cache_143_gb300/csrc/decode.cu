@@ -93,38 +93,16 @@ struct SmemTail {
 
 // The producer warp of both decode kernels: the warp fetches the block ids of
 // 32 chunks at a time (lane i: chunk base + i, one coalesced load). Per 16-key
-// chunk, K and V are each one contiguous run of the pool. Runs of 4 KB and
-// more go as one bulk async copy each, issued by lane 0 (completing on the
-// stage's mbarrier by transaction bytes); smaller runs (E4M3 codes) go as
-// 16-byte asynchronous copies spread over the 32 lanes, each lane's copies
-// completing one arrival on the stage's mbarrier. The bulk-copy engine
-// completes about as many copies per second whatever their size, so small
-// runs would halve the bandwidth.
-template <class G>
-struct ProducerKind {
-  static constexpr bool kLanes = G::kChunkBytes < 4096;  // lane copies, else bulk
-  static constexpr unsigned kArrivals = kLanes ? 32u : 1u;  // full-barrier count
-};
-
-__device__ __forceinline__ void lane_copy16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-               "l"(gmem_src)
-               : "memory");
-}
-
-// One arrival on `bar` once every earlier lane_copy16 of this thread has landed.
-__device__ __forceinline__ void lane_copies_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
+// chunk, K and V are each one contiguous run of the pool, moved by one bulk
+// async copy each that completes on the stage's mbarrier by transaction
+// bytes. The producer handles a group of chunks per step (lane i waits for
+// the stage of chunk c0 + i and issues its copies), so that the waits and the
+// copy issue of a group overlap; one chunk per step left only about two
+// chunks in flight.
 template <class G>
 __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
                                         int r, int kvh, int k_begin, int nch, int lane) {
-  constexpr bool kLanes = ProducerKind<G>::kLanes;
-  // chunks handled per step: lane i < kGroup waits for the stage of chunk
-  // c0 + i and (bulk copies) issues it, so the waits and the copy issue of a
-  // group overlap instead of running one chunk after another
+  // chunks handled per step (half the ring, at most 8)
   constexpr int kGroup = G::kStages / 2 < 8 ? G::kStages / 2 : 8;
   static_assert(32 % kGroup == 0, "groups must tile the 32 chunks of a block-id fetch");
   const unsigned full = 0xffffffffu;
@@ -156,20 +134,7 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
         break;
       }
       const int64_t off = __shfl_sync(full, off_lane, (g0 + lane) & 31);
-      if constexpr (kLanes) {
-        // every lane copies its 16-byte pieces of each chunk of the group
-        for (int i = 0; i < gn; ++i) {
-          const int ci = base + g0 + i;
-          const int64_t oi = __shfl_sync(full, off, i);
-          uint8_t* dst = ring + (ci % G::kStages) * G::kStageBytes;
-#pragma unroll
-          for (int k = lane * 16; k < G::kChunkBytes; k += 32 * 16) {
-            lane_copy16(dst + k, p.k_pool + oi + k);
-            lane_copy16(dst + G::kChunkBytes + k, p.v_pool + oi + k);
-          }
-          lane_copies_arrive(&tail->full[ci % G::kStages]);
-        }
-      } else if (mine) {
+      if (mine) {
         uint8_t* dst = ring + stage * G::kStageBytes;
         mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
         bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
@@ -179,9 +144,7 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
     }
   }
   // drain: every issued copy has landed before the CTA may exit
-  if constexpr (kLanes) {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (lane == 0) {
+  if (lane == 0) {
     for (int c = issued - G::kStages > 0 ? issued - G::kStages : 0; c < issued; ++c)
       mbar_wait(&tail->full[c % G::kStages], (c / G::kStages) & 1, p.err);
   }
@@ -233,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tail->full[i], ProducerKind<G>::kArrivals);
+      mbar_init(&tail->full[i], 1);
       mbar_init(&tail->empty[i], HG);  // one arrival per head group
     }
     tail->abort = 0;
@@ -502,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tail->full[i], ProducerKind<G>::kArrivals);
+      mbar_init(&tail->full[i], 1);
       mbar_init(&tail->empty[i], 1);
     }
     tail->abort = 0;
