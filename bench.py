@@ -36,6 +36,23 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def combine_ranks(times, units, world, device):
+    """Whole-job view of a replicated step: every time is the slowest rank's
+    (max over ranks) and the work is what all ranks processed together (sum
+    over ranks; each rank runs its own seeded batch, so the ranks' units
+    differ). world == 1 returns the inputs."""
+    times = [float(x) for x in times]
+    if world == 1:
+        return times, float(units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(times, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.cpu()], float(u.cpu()[0])
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -226,18 +243,15 @@ def run_libpa(args):
         raise RuntimeError("device error in the timed region")
     ms = t0.elapsed_time(t1) / args.steps
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms, fwd_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, fwd_ms = float(t[0]), float(t[1])
+    (ms, fwd_ms), total_kv = combine_ranks((ms, fwd_ms), kv_bytes, world, dev)
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside
     e2e = run_e2e(args, w, step, dev, kv_bytes, world)
 
     peak, peak_kind = load_peaks()
-    achieved = kv_bytes / (fwd_ms * 1e-3) / 1e9
+    achieved = total_kv / world / (fwd_ms * 1e-3) / 1e9  # per GPU
     line = {
-        "metric": METRIC, "value": round(kv_bytes * world / (ms * 1e-3) / 1e9, 2),
+        "metric": METRIC, "value": round(total_kv / (ms * 1e-3) / 1e9, 2),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -571,12 +585,8 @@ def run_e2e(args, w, step, dev, kv_bytes, world):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-    return {"value": round(kv_bytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    (ms,), total_kv = combine_ranks((ms,), kv_bytes, world, dev)
+    return {"value": round(total_kv / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "ms_per_step": round(ms, 5), "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
 
