@@ -29,11 +29,18 @@
 //                P as bf16 pairs over S; O is rescaled in TMEM only when the
 //                running max grows by more than 2^8 (the stale max is otherwise
 //                kept, which is exact algebra); epilogue O / l.
+// E4M3 pools: S runs on E4M3 tensor-core operands at D = 128 (kind::f8f6f4:
+// the K codes as stored, the query as the sum of three E4M3 terms after a
+// power-of-two scale, ~2^-12 relative), while V is widened to f16 in place by
+// two converter warps and P.V stays on f16 operands (P keeps f16 range).
+// At D = 64 both K and V are widened and every MMA is f16.
 // Every wait is bounded; a timeout sets the error word and the CTA unwinds
 // (waits for its copies and MMAs, frees TMEM) without writing output.
 #include <cudaTypedefs.h>
 
 #include <mutex>
+
+#include <cuda_fp8.h>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -65,16 +72,23 @@ struct Smem {
   static constexpr int kStages = D == 128 ? 2 : 4;     // KV tiles in flight
   static constexpr int kChunkBytes = kN * 128;         // 128 rows x 64 bf16 (one swizzle column)
   static constexpr int kChunks = D / 64;
-  static constexpr int kQBytes = kM * D * 2;           // one Q tile
-  static constexpr int kKVBytes = kN * D * 2;          // one K or V tile
+  static constexpr int kQBytes = kM * D * 2;           // one Q tile (bf16, as loaded)
+  static constexpr int kKVBytes = kN * D * 2;          // one K or V tile (16-bit)
+  // E4M3 pools at D = 128: S runs on E4M3 operands. K tiles stay E4M3 codes
+  // (128-byte rows, 128-byte swizzle, 16 KB); each Q tile becomes three E4M3
+  // tiles (q ~ hi + mid + lo) written over and after its bf16 copy (48 KB).
+  static constexpr bool kF8S = F8 && D == 128;
+  static constexpr int kQPart = kM * 128;              // one E4M3 Q tile
+  static constexpr int kQRegion = kF8S ? 3 * kQPart : kQBytes;
+  static constexpr int kKBytes = kF8S ? kN * D : kKVBytes;
   static constexpr int kOffQ = 0;                      // Q_A, then Q_B
-  static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  // E4M3 pools: the tile of codes (rows of D bytes) of stage st lands in the
-  // upper half of its own f16 stage for D = 128 and is widened in place (row r
-  // of codes occupies exactly the bytes of row r of the upper 64-column chunk,
-  // so a row's codes are read before its second half is written); for D = 64
-  // each stage has a staging tile of its own.
+  static constexpr int kOffK = 2 * kQRegion;
+  static constexpr int kOffV = kOffK + kStages * kKBytes;
+  // E4M3 V (and K for D = 64): the tile of codes (rows of D bytes) of stage st
+  // lands in the upper half of its own f16 stage for D = 128 and is widened in
+  // place (row r of codes occupies exactly the bytes of row r of the upper
+  // 64-column chunk, so a row's codes are read before its second half is
+  // written); for D = 64 each stage has a staging tile of its own.
   static constexpr bool kInPlace = F8 && D == 128;
   static constexpr int kK8Bytes = F8 && !kInPlace ? kN * D : 0;  // per stage
   static constexpr int kOffK8 = kOffV + kStages * kKVBytes;
@@ -83,9 +97,10 @@ struct Smem {
   static constexpr int kBytes = kOffBar + 256;
   static constexpr int kAlloc = kBytes + 1024;  // the base is rounded up to 1024 B
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB per-block limit");
-  __host__ __device__ static constexpr int k8(int st) {
-    return kInPlace ? kOffK + st * kKVBytes + kKVBytes / 2 : kOffK8 + st * kK8Bytes;
-  }
+  static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kKBytes % 1024 == 0,
+                "128-byte-swizzled tiles start on 1024-byte boundaries");
+  // where the E4M3 codes of stage st land (K only for D = 64)
+  __host__ __device__ static constexpr int k8(int st) { return kOffK8 + st * kK8Bytes; }
   __host__ __device__ static constexpr int v8(int st) {
     return kInPlace ? kOffV + st * kKVBytes + kKVBytes / 2 : kOffV8 + st * kK8Bytes;
   }
@@ -204,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       // bf16: completed by the TMA bytes; E4M3: by the two converter warps
-      mbar_init(&bars->k_full[s], F8 ? 2 : 1);
+      mbar_init(&bars->k_full[s], F8 && !S::kF8S ? 2 : 1);
       mbar_init(&bars->v_full[s], F8 ? 2 : 1);
       mbar_init(&bars->k_empty[s], 1);
       mbar_init(&bars->v_empty[s], 1);
@@ -246,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bars->q_full, nq * S::kQBytes);
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < S::kChunks; ++c)
-          tc::tma_load_4d(smem + S::kOffQ + t * S::kQBytes + c * S::kChunkBytes, &tmap_q,
+          tc::tma_load_4d(smem + S::kOffQ + t * S::kQRegion + c * S::kChunkBytes, &tmap_q,
                           c * 64, 0, kvh, q_begin + q0[t], &bars->q_full);
     }
     const int nbt = kN / p.B;  // blocks per KV tile (<= 8)
@@ -273,11 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = ((F8 ? blk_lane : blk) * p.Hkv + kvh) * p.B;
       // bf16: boxes of 64 columns into the swizzled stage; E4M3: one box of
       // D codes x B keys per block into the stage's tile of codes
-      const int k_dst = F8 ? S::k8(st) + lane * p.B * D
-                           : S::kOffK + st * S::kKVBytes + box_chunk * S::kChunkBytes +
+      // K: bf16 — 64-column boxes into the swizzled stage; E4M3, D = 128 —
+      // one box of 128 codes x B keys per block straight into the swizzled
+      // stage (the MMA reads the codes); E4M3, D = 64 — into the code tile
+      const int k_dst = S::kF8S ? S::kOffK + st * S::kKBytes + lane * p.B * 128
+                        : F8    ? S::k8(st) + lane * p.B * D
+                                : S::kOffK + st * S::kKBytes + box_chunk * S::kChunkBytes +
+                                      box_block * p.B * 128;
+      const int v_dst = F8 ? S::v8(st) + lane * p.B * D
+                           : S::kOffV + st * S::kKVBytes + box_chunk * S::kChunkBytes +
                                  box_block * p.B * 128;
-      const int v_dst = F8 ? S::v8(st) + lane * p.B * D : k_dst - S::kOffK + S::kOffV;
-      uint64_t* kbar = F8 ? &bars->k8_full[st] : &bars->k_full[st];
+      uint64_t* kbar = F8 && !S::kF8S ? &bars->k8_full[st] : &bars->k_full[st];
       uint64_t* vbar = F8 ? &bars->v8_full[st] : &bars->v_full[st];
       // K of tile j: the stage is free once the S MMAs of tile j - kStages are
       // done (for E4M3 this implies its codes were widened, and read, before)
@@ -311,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_wait(&bars->q_full, 0, p.err);
       for (int j = issued_k - kStages > 0 ? issued_k - kStages : 0; j < issued_k; ++j)
-        mbar_wait(F8 ? &bars->k8_full[j % kStages] : &bars->k_full[j % kStages],
+        mbar_wait(F8 && !S::kF8S ? &bars->k8_full[j % kStages] : &bars->k_full[j % kStages],
                   (j / kStages) & 1, p.err);
       for (int j = issued_v - kStages > 0 ? issued_v - kStages : 0; j < issued_v; ++j)
         mbar_wait(F8 ? &bars->v8_full[j % kStages] : &bars->v_full[j % kStages],
@@ -324,15 +345,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_o = tc::idesc_16bit_f32(kM, D, false, true, F8);
       bool ok = mbar_wait(F8 ? &bars->q_conv : &bars->q_full, 0, p.err);
       auto issue_s = [&](int t, int j) {
-        const uint8_t* qs = smem + S::kOffQ + t * S::kQBytes;
-        const uint8_t* ks = smem + S::kOffK + (j % kStages) * S::kKVBytes;
+        const uint8_t* qs = smem + S::kOffQ + t * S::kQRegion;
+        const uint8_t* ks = smem + S::kOffK + (j % kStages) * S::kKBytes;
+        if constexpr (S::kF8S) {
+          // S = (q_hi + q_mid + q_lo) . k on E4M3 operands: per Q part, four
+          // K = 32 steps along a 128-byte row (32 bytes each)
+          constexpr uint32_t idesc_s8 = tc::idesc_e4m3_f32(kM, kN);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint64_t a =
-              tc::smem_desc_sw128(qs + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
-          const uint64_t b =
-              tc::smem_desc_sw128(ks + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tmem + t * kN, a, b, idesc_s, k > 0);
+          for (int part = 0; part < 3; ++part)
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+              const uint64_t a = tc::smem_desc_sw128(qs + part * S::kQPart + k * 32, 16, 1024);
+              const uint64_t b = tc::smem_desc_sw128(ks + k * 32, 16, 1024);
+              tc::mma_e4m3_ss(tmem + t * kN, a, b, idesc_s8, part > 0 || k > 0);
+            }
+        } else {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a =
+                tc::smem_desc_sw128(qs + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
+            const uint64_t b =
+                tc::smem_desc_sw128(ks + (k >> 2) * S::kChunkBytes + (k & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tmem + t * kN, a, b, idesc_s, k > 0);
+          }
         }
         tc::mma_commit(&bars->s_full[t]);
       };
@@ -414,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < ntk_all && ok; ++j) {
       const int st = j % kStages;
-      for (int kv = 0; kv < 2 && ok; ++kv) {
+      // D = 128: only V is widened (S reads the K codes); D = 64: K and V
+      for (int kv = S::kF8S ? 1 : 0; kv < 2 && ok; ++kv) {
         // the codes landed; the producer issued them only once the stage was
         // free (its MMAs of tile j - kStages done)
         uint64_t* landed = kv ? &bars->v8_full[st] : &bars->k8_full[st];
@@ -456,13 +492,91 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float score_scale = p.scale_log2;  // log2(e) * scale (* k_scale for E4M3)
     if (F8) {
-      // The MMAs run on f16 operands: this thread converts its own Q row in
-      // place, pre-scaled by 2^e so that the row's largest magnitude lands in
-      // [2^14, 2^15) (exact: a power of two), and divides the scores by 2^e.
+      // E4M3 pools. D = 64: the MMAs run on f16 operands; this thread
+      // converts its own Q row in place, pre-scaled by 2^e so that the row's
+      // largest magnitude lands in [2^14, 2^15) (exact: a power of two), and
+      // divides the scores by 2^e. D = 128: see the E4M3 split below.
       if (my_ntk > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.err));
-        if (ok) {
-          uint8_t* qrow = smem + S::kOffQ + t * S::kQBytes + row * 128;
+        if constexpr (S::kF8S) {
+          if (ok) {
+            // S runs on E4M3 operands: this thread's row becomes three E4M3
+            // rows, q * 2^e ~ hi + mid + lo (each the E4M3 rounding of what the
+            // earlier terms leave), after an exact power-of-two scale that puts
+            // the row's largest magnitude in [2^7, 2^8); the scores are divided
+            // by 2^e. The thread reads its whole bf16 row first: hi and mid
+            // take the bytes of that row in the two bf16 chunks, lo the tile's
+            // third 16 KB.
+            uint8_t* tq = smem + S::kOffQ + t * S::kQRegion;
+            const int sw = row & 7;
+            uint4 bq[2][8];
+            float amax = 0.f;
+  #pragma unroll
+            for (int c = 0; c < 2; ++c)
+  #pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                bq[c][q] = *reinterpret_cast<const uint4*>(tq + c * S::kChunkBytes + row * 128 +
+                                                           ((q ^ sw) << 4));
+                float f[8];
+                bf16x8_to_f32(bq[c][q], f);
+  #pragma unroll
+                for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+              }
+            int e2 = 0;
+            if (amax > 0.f) {
+              const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+              e2 = min(100, max(-120, 7 - ex));
+            }
+            const float up = __uint_as_float((uint32_t)(e2 + 127) << 23);
+            score_scale *= __uint_as_float((uint32_t)(127 - e2) << 23);
+            auto e4m3x2 = [](float a, float b) -> uint32_t {  // a in the low byte
+              return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                                        __NV_E4M3);
+            };
+            auto back = [](uint32_t codes, float& a, float& b) {  // exact
+              uint32_t h;
+              asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                  "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+                  : "=r"(h)
+                  : "r"(codes));
+              const __half2 x = *reinterpret_cast<const __half2*>(&h);
+              a = __low2float(x);
+              b = __high2float(x);
+            };
+  #pragma unroll
+            for (int g = 0; g < 8; ++g) {  // 16 dims: 16g .. 16g + 15
+              float f[16];
+              bf16x8_to_f32(bq[g >> 2][2 * (g & 3)], *reinterpret_cast<float(*)[8]>(f));
+              bf16x8_to_f32(bq[g >> 2][2 * (g & 3) + 1], *reinterpret_cast<float(*)[8]>(f + 8));
+              uint32_t part[3][4];
+  #pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                uint32_t words[3] = {0u, 0u, 0u};
+  #pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {  // two pairs of dims per 32-bit word
+                  float x0 = f[4 * w + 2 * hb] * up, x1 = f[4 * w + 2 * hb + 1] * up;
+  #pragma unroll
+                  for (int pi = 0; pi < 3; ++pi) {
+                    const uint32_t c2 = e4m3x2(x0, x1);
+                    words[pi] |= c2 << (16 * hb);
+                    float y0, y1;
+                    back(c2, y0, y1);
+                    x0 -= y0;
+                    x1 -= y1;
+                  }
+                }
+  #pragma unroll
+                for (int pi = 0; pi < 3; ++pi) part[pi][w] = words[pi];
+              }
+  #pragma unroll
+              for (int pi = 0; pi < 3; ++pi)
+                *reinterpret_cast<uint4*>(tq + pi * S::kQPart + row * 128 + ((g ^ sw) << 4)) =
+                    make_uint4(part[pi][0], part[pi][1], part[pi][2], part[pi][3]);
+            }
+            tc::fence_proxy_async_smem();
+          }
+        } else if (ok) {
+          uint8_t* qrow = smem + S::kOffQ + t * S::kQRegion + row * 128;
           float amax = 0.f;
 #pragma unroll
           for (int c = 0; c < S::kChunks; ++c)
@@ -713,7 +827,8 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   }
   // K and V as rows [(block * Hkv + head) * B + offset][D]. bf16: box = 64
   // dims x B rows, 128-byte swizzled (the MMA operand layout); E4M3: box =
-  // D codes x B rows, unswizzled (the converter warps read it).
+  // D codes x B rows, unswizzled where the converter warps read it (V; K for
+  // D = 64) and 128-byte swizzled where the MMA reads the codes (K, D = 128).
   {
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.num_blocks * p.Hkv * p.B};
     cuuint64_t strides[1] = {(cuuint64_t)D * (F8 ? 1 : 2)};
@@ -722,8 +837,9 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
     const CUtensorMapDataType dt =
         F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUtensorMapSwizzle sw = F8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    const CUtensorMapSwizzle sw_k = Smem<D, F8>::kF8S ? CU_TENSOR_MAP_SWIZZLE_128B : sw;
     if (encode(&tk, dt, 2, const_cast<void*>(L.k_pool), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw_k, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     if (encode(&tv, dt, 2, const_cast<void*>(L.v_pool), dims, strides, box, es,
