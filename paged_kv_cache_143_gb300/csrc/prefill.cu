@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S = (q_hi + q_mid + q_lo) . k on E4M3 operands: per Q part, four
           // K = 32 steps along a 128-byte row (32 bytes each)
           constexpr uint32_t idesc_s8 = tc::idesc_e4m3_f32(kM, kN);
-#pragma unroll
+#pragma unroll 1
           for (int part = 0; part < 3; ++part)
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) {
