@@ -11,22 +11,24 @@
 // Design (HBM-bound by construction):
 //  - one CTA per (key split, kv head, request): all g query heads of the GQA
 //    group that share the kv head are served from one read of the KV;
-//  - warp 4 is a producer: the warp fetches the block ids of 32 chunks at a
-//    time and one lane issues a 1-D bulk async copy (cp.async.bulk, completes
-//    on an mbarrier) per 16-key chunk of K and of V into an 8-stage shared
-//    ring; a (block, kv head) is contiguous in the pool, so every chunk is one
-//    contiguous 16*D*elt copy;
-//  - warps 0..3 compute. With g <= 4 each warp owns every 4th chunk for all
-//    g heads; with g = 8 (16) the warps split into 2 (4) head groups of 4
-//    heads and each chunk is consumed by one warp of every head group. Lane
-//    (a, b) = (lane/8, lane%8) handles keys a, a+4, a+8, a+12 of the chunk and
-//    a fixed 1/8 of the head dimension, so a quarter-warp reads 128
+//  - warp 4 is a producer: per 16-key chunk, K and V are each one contiguous
+//    run of the pool (a (block, kv head) is contiguous), moved by one bulk
+//    async copy (cp.async.bulk, completing on the stage's mbarrier) into a
+//    64 KB ring (8 bf16 / 16 E4M3 stages). The warp fetches the block ids of
+//    32 chunks at a time and handles a group of chunks per step, lane i
+//    waiting for and issuing chunk c0 + i, so waits and copy issue overlap;
+//  - warps 0..3 compute, each owning every 4th chunk. g = 1 (decode_kernel):
+//    lane (a, b) = (lane/8, lane%8) handles keys a, a+4, a+8, a+12 of the
+//    chunk and a fixed 1/8 of the head dimension, so a quarter-warp reads 128
 //    contiguous bytes of one key row (no bank conflicts); the dot products
 //    use packed fp32 multiply-adds and finish with 3 xor-shuffles; P*V
 //    accumulates in registers and is reduced across the key lanes once per
-//    split;
+//    split. g >= 2 (decode_mma_kernel, described at its definition):
+//    warp-level tensor-core products with the g query heads as rows;
 //  - the warps merge through shared memory; one split writes bf16 output
 //    directly, several write fp32 partials (o, m, l) for the merge kernel.
+//    A request in a shared-prefix group attends only to its keys after the
+//    prefix and writes its splits after the prefix pieces' slots.
 // FP8 E4M3 codes are widened in registers (exact); k_scale is folded into the
 // query scale and v_scale into the output.
 #include "pa_device.cuh"
