@@ -49,6 +49,8 @@ CASES = [
     ([7, 513, 2048], 32, 2, 128, 16, "bf16"),           # g = 16
     ([9, 130, 77], 8, 8, 64, 64, "fp8"),
     ([17, 1111], 4, 1, 64, 32, "bf16"),                 # g = 4, D = 64
+    ([3, 47, 1500], 32, 2, 128, 16, "fp8"),             # g = 16: hi and mid in two products
+    ([11, 260, 33], 8, 4, 64, 32, "fp8"),               # g = 2, D = 64
 ]
 
 
@@ -59,6 +61,19 @@ def test_decode_shapes(cuda_device, case, max_splits):
     w = workloads.build(seq, [1] * len(seq), Hq, Hkv, D, B, kv_dtype=dt, seed=sum(seq) + Hq,
                         device=cuda_device, pool_blocks=None)
     run_and_check(w, cuda_device, max_splits=max_splits)
+
+
+@pytest.mark.parametrize("g", [4, 16])
+def test_decode_fp8_query_magnitudes_per_head(cuda_device, g):
+    """E4M3 pools: every query head gets its own power-of-two scale before it
+    is split into E4M3 parts, so heads of very different size, and an
+    all-zero head, keep their accuracy."""
+    Hkv = 2
+    w = workloads.build([5, 333, 1200], [1, 1, 1], Hq=g * Hkv, Hkv=Hkv, D=128, B=16,
+                        kv_dtype="fp8", seed=77, device=cuda_device)
+    mult = torch.tensor([0.0, 1e-3, 1.0, 7.5] * (g * Hkv // 4), device=w.q.device)
+    w.q.mul_(mult.view(1, -1, 1).to(w.q.dtype))
+    run_and_check(w, cuda_device)
 
 
 def test_decode_long_context_requests(cuda_device):
