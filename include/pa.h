@@ -151,6 +151,7 @@ size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t 
  * with q_len == 0 are not touched. Requests may appear in any order.
  * Host checks: qsl_host must be non-decreasing with qsl_host[R] == T, and
  * 1 <= q_len <= seq_len <= max_blocks * block_size for every request with
+ * q_len > 0, and a pool with at least one block when any request has
  * q_len > 0; otherwise PA_ERR_INVALID.
  */
 pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,

@@ -34,6 +34,7 @@
 #include "pa_device.cuh"
 #include "pa_internal.h"
 #include "pa_kernels.h"
+#include "tc_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -100,10 +101,13 @@ struct SmemTail {
 // bytes. The producer handles a group of chunks per step (lane i waits for
 // the stage of chunk c0 + i and issues its copies), so that the waits and the
 // copy issue of a group overlap; one chunk per step left only about two
-// chunks in flight.
-template <class G>
+// chunks in flight. kTma: the same runs move as TMA tensor boxes (16 rows of
+// 128 codes, 128-byte swizzle) through the maps tk and tv, which view a pool
+// as [block][kv head * B + offset][128].
+template <class G, bool kTma>
 __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
-                                        int r, int kvh, int k_begin, int nch, int lane) {
+                                        int r, int kvh, int k_begin, int nch, int lane,
+                                        const CUtensorMap* tk, const CUtensorMap* tv) {
   // chunks handled per step (half the ring, at most 8)
   constexpr int kGroup = G::kStages / 2 < 8 ? G::kStages / 2 : 8;
   static_assert(32 % kGroup == 0, "groups must tile the 32 chunks of a block-id fetch");
@@ -119,9 +123,11 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
     const bool bad = c_lane < nch && (blk_lane < 0 || blk_lane >= p.num_blocks);
     if (__any_sync(full, bad) && lane == 0) raise_error(p.err, kErrBounds);
     if (bad) blk_lane = 0;  // read a valid block; the call's output is then unspecified
-    // byte offset of each lane's chunk in the pool (one contiguous run of K, of V)
+    // byte offset of each lane's chunk in the pool (one contiguous run of K, of
+    // V), or its TMA coordinates (row within the block, block)
     const int64_t off_lane = ((int64_t)blk_lane * p.Hkv + kvh) * head_stride +
                              (int64_t)(key_lane % p.B) * G::kRowBytes;
+    const int y_lane = kvh * p.B + key_lane % p.B;
     const int n = min(32, nch - base);
     for (int g0 = 0; g0 < n; g0 += kGroup) {
       const int gn = min(kGroup, n - g0);
@@ -135,12 +141,23 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
         if (lane == 0) tail->abort = 1;
         break;
       }
-      const int64_t off = __shfl_sync(full, off_lane, (g0 + lane) & 31);
-      if (mine) {
-        uint8_t* dst = ring + stage * G::kStageBytes;
-        mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
-        bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
-        bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
+      if constexpr (kTma) {
+        const int y = __shfl_sync(full, y_lane, (g0 + lane) & 31);
+        const int z = __shfl_sync(full, blk_lane, (g0 + lane) & 31);
+        if (mine) {
+          uint8_t* dst = ring + stage * G::kStageBytes;
+          mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
+          tc::tma_load_3d(dst, tk, 0, y, z, &tail->full[stage]);
+          tc::tma_load_3d(dst + G::kChunkBytes, tv, 0, y, z, &tail->full[stage]);
+        }
+      } else {
+        const int64_t off = __shfl_sync(full, off_lane, (g0 + lane) & 31);
+        if (mine) {
+          uint8_t* dst = ring + stage * G::kStageBytes;
+          mbar_arrive_expect_tx(&tail->full[stage], G::kStageBytes);
+          bulk_g2s(dst, p.k_pool + off, G::kChunkBytes, &tail->full[stage]);
+          bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
+        }
       }
       issued = base + g0 + gn;
     }
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   __syncthreads();
 
   if (warp == kConsumerWarps) {
-    produce<G>(p, ring, tail, r, kvh, k_begin, nch, lane);
+    produce<G, false>(p, ring, tail, r, kvh, k_begin, nch, lane, nullptr, nullptr);
     return;
   }
 
@@ -419,16 +436,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 // E4M3 pools run f16 MMAs: the codes widen exactly to f16, and each query row
 // is pre-scaled by a power of two into [2^14, 2^15) before its f16 rounding
 // (undone in the score scale), so f16 range never limits the queries.
+// E4M3 at D = 128: the stages arrive as TMA tensor boxes with the 128-byte
+// swizzle (16-byte chunk c of row r stored at chunk c ^ (r & 7)). In linear
+// rows the lanes that hold different keys of the same columns hit the same
+// banks (rows are 128 B apart); swizzled, a lane reads the chunks 2 tig and
+// 2 tig + 1 of its K row (the head-dimension permutation becomes: k-step
+// pair j of lane tig = dims 32 tig + 8 j .. +7) and chunk grp of its V rows,
+// and every 16-byte load of a quarter-warp falls on distinct banks.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
   using G = Geo<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
   constexpr int KJ = D / 32;       // pairs of k-steps
   constexpr int DG = D / 8;        // output dims per lane group = n-tiles of O
+  constexpr bool kSw = FP8 && D == 128;  // swizzled stages (TMA tensor copies)
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  float* comb_o = reinterpret_cast<float*>(smem + kStages * G::kStageBytes);  // [4][16][D]
+  if constexpr (kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;  // 1024-byte aligned
+  float* comb_o = reinterpret_cast<float*>(ring + kStages * G::kStageBytes);  // [4][16][D]
   float* comb_m = comb_o + kConsumerWarps * kRows * D;                       // [4][16]
   float* comb_l = comb_m + kConsumerWarps * kRows;                           // [4][16]
   SmemTail* tail = reinterpret_cast<SmemTail*>(comb_l + kConsumerWarps * kRows);
@@ -475,7 +503,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
   }
   __syncthreads();
   if (warp == kConsumerWarps) {
-    produce<G>(p, ring, tail, r, kvh, k_begin, nch, lane);
+    if (kSw && lane == 0) {
+      tc::prefetch_tensormap(&tmap_k);
+      tc::prefetch_tensormap(&tmap_v);
+    }
+    produce<G, kSw>(p, ring, tail, r, kvh, k_begin, nch, lane, &tmap_k, &tmap_v);
     return;
   }
 
@@ -493,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
       for (int j = 0; j < KJ; ++j) {
         if (row < g) {
           const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              p.q + ((int64_t)qs * p.Hq + hq0 + row) * D + 32 * j + 8 * tig));
+              p.q + ((int64_t)qs * p.Hq + hq0 + row) * D + (kSw ? 32 * tig + 8 * j : 32 * j + 8 * tig)));
           bf16x8_to_f32(v, qf[ri][j]);
         } else {
 #pragma unroll
@@ -550,15 +582,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
           : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
           : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
   };
+  // 8 E4M3 codes -> four f16 pairs (exact)
+  auto widen8 = [](uint32_t x, uint32_t y, uint32_t* w) {
+    asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+        : "r"(x), "r"(y));
+  };
   // 8 consecutive elements of a row -> four 16-bit pairs
-  auto load8 = [](const uint8_t* src, uint32_t (&w)[4]) {
+  auto load8 = [&](const uint8_t* src, uint32_t (&w)[4]) {
     if (FP8) {
       const uint2 v = *reinterpret_cast<const uint2*>(src);
-      asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
-          "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
-          "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
-          : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-          : "r"(v.x), "r"(v.y));
+      widen8(v.x, v.y, w);
     } else {
       const uint4 v = *reinterpret_cast<const uint4*>(src);
       w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
@@ -588,12 +624,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
     for (int t = 0; t < 2; ++t) {
       s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
       const uint8_t* krow = Ks + (8 * t + grp) * G::kRowBytes;
+      if constexpr (kSw) {
+        // k-step pairs 2h, 2h+1 of lane tig: dims 32 tig + 16 h .. +15, the
+        // 16-byte chunk 2 tig + h of row grp, stored at chunk ^ grp
 #pragma unroll
-      for (int j = 0; j < KJ; ++j) {
-        uint32_t kw[4];
-        load8(krow + (32 * j + 8 * tig) * G::kElt, kw);
-        mma(s[t], qa[j][0][0], qa[j][1][0], qa[j][0][1], qa[j][1][1], kw[0], kw[1]);
-        mma(s[t], qa[j][0][2], qa[j][1][2], qa[j][0][3], qa[j][1][3], kw[2], kw[3]);
+        for (int h = 0; h < KJ / 2; ++h) {
+          const uint4 x =
+              *reinterpret_cast<const uint4*>(krow + (((2 * tig + h) ^ grp) << 4));
+          uint32_t kw[4];
+          widen8(x.x, x.y, kw);
+          mma(s[t], qa[2 * h][0][0], qa[2 * h][1][0], qa[2 * h][0][1], qa[2 * h][1][1], kw[0],
+              kw[1]);
+          mma(s[t], qa[2 * h][0][2], qa[2 * h][1][2], qa[2 * h][0][3], qa[2 * h][1][3], kw[2],
+              kw[3]);
+          widen8(x.z, x.w, kw);
+          mma(s[t], qa[2 * h + 1][0][0], qa[2 * h + 1][1][0], qa[2 * h + 1][0][1],
+              qa[2 * h + 1][1][1], kw[0], kw[1]);
+          mma(s[t], qa[2 * h + 1][0][2], qa[2 * h + 1][1][2], qa[2 * h + 1][0][3],
+              qa[2 * h + 1][1][3], kw[2], kw[3]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < KJ; ++j) {
+          uint32_t kw[4];
+          load8(krow + (32 * j + 8 * tig) * G::kElt, kw);
+          mma(s[t], qa[j][0][0], qa[j][1][0], qa[j][0][1], qa[j][1][1], kw[0], kw[1]);
+          mma(s[t], qa[j][0][2], qa[j][1][2], qa[j][0][3], qa[j][1][3], kw[2], kw[3]);
+        }
       }
     }
     // scale, mask, online softmax of rows grp (c0, c1) and grp + 8 (c2, c3)
@@ -655,13 +712,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_mma_kernel(DecodeParams p)
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int kr = 2 * tig + (i & 1) + 8 * (i >> 1);
-      const uint8_t* vrow = Vs + kr * G::kRowBytes + DG * grp * G::kElt;
+      if constexpr (kSw) {  // the 16-byte chunk grp of row kr, stored at grp ^ (kr & 7)
+        const uint4 x =
+            *reinterpret_cast<const uint4*>(Vs + kr * G::kRowBytes + ((grp ^ (kr & 7)) << 4));
+        widen8(x.x, x.y, &vw[i][0]);
+        widen8(x.z, x.w, &vw[i][4]);
+      } else {
+        const uint8_t* vrow = Vs + kr * G::kRowBytes + DG * grp * G::kElt;
 #pragma unroll
-      for (int h = 0; h < DG / 8; ++h) {
-        uint32_t w4[4];
-        load8(vrow + 8 * h * G::kElt, w4);
+        for (int h = 0; h < DG / 8; ++h) {
+          uint32_t w4[4];
+          load8(vrow + 8 * h * G::kElt, w4);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
+          for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
+        }
       }
       if (key0 + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
 #pragma unroll
@@ -811,13 +875,35 @@ cudaError_t launch_decode_t(const DecodeParams& p, int R, int max_splits, cudaSt
 
 template <int D, bool FP8>
 cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
-  constexpr int smem = Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
+  constexpr bool kSw = FP8 && D == 128;
+  constexpr int smem = (kSw ? 1024 : 0) + Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
                        kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
+  CUtensorMap tk{}, tv{};  // unused by the unswizzled kernels
+  if constexpr (kSw) {
+    auto encode = tensor_map_encoder();
+    if (!encode) return cudaErrorNotSupported;
+    if (p.num_blocks < 1) return cudaErrorInvalidValue;
+    // a pool as [block][kv head * B + offset][128 codes]; one box = one 16-key
+    // chunk of one kv head, 128-byte swizzled
+    cuuint64_t dims[3] = {128, (cuuint64_t)p.Hkv * p.B, (cuuint64_t)p.num_blocks};
+    cuuint64_t strides[2] = {128, (cuuint64_t)p.Hkv * p.B * 128};
+    cuuint32_t box[3] = {128, (cuuint32_t)kChunk, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.k_pool), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        encode(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.v_pool), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   auto k = decode_mma_kernel<D, FP8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(max_splits, p.Hkv, R);
-  k<<<grid, kThreads, smem, s>>>(p);
+  k<<<grid, kThreads, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -176,6 +176,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   };
 
   if (n_dec > 0) {
+    if (pool->num_blocks == 0) return PA_ERR_INVALID;  // no block a table could name
     pa::DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.out = static_cast<__nv_bfloat16*>(out);

@@ -1,6 +1,8 @@
 // pa_internal.h — host-side helpers shared by the libpa translation units.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,5 +39,9 @@ inline pa_status launch_status() {
 
 // Shape checks shared by every entry point that takes a pool.
 pa_status check_pool(const pa_kv_pool* pool);
+
+// The driver's cuTensorMapEncodeTiled (looked up once); nullptr if the driver
+// does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 }  // namespace pa

@@ -792,20 +792,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------- host launch
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
 template <int D, bool F8>
 cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   auto encode = tensor_map_encoder();

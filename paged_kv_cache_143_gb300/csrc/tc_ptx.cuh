@@ -1,7 +1,8 @@
 // tc_ptx.cuh — thin inline-PTX wrappers for the sm_100-family tensor-core path
-// used by the prefill kernel: TMA tensor loads, tensor-memory (TMEM)
-// allocation and access, 5th-generation MMA (tcgen05.mma) with shared-memory
-// matrix descriptors, and the fences that order them.
+// of the prefill kernel (the TMA loads also serve the E4M3 decode kernel): TMA
+// tensor loads, tensor-memory (TMEM) allocation and access, 5th-generation MMA
+// (tcgen05.mma) with shared-memory matrix descriptors, and the fences that
+// order them.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap
@@ -20,6 +21,15 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 

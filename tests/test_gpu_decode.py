@@ -180,3 +180,8 @@ def test_forward_host_checks(cuda_device):
                    torch.empty((2, 3, 64), dtype=torch.bfloat16, device=cuda_device),
                    step.qsl, step.seq, w.qsl, w.seq_lens, step.gathered, step.pool, w.scale, 1)
     assert e.value.status == pa.PA_ERR_UNSUPPORTED
+    empty = pa.KVPool(step.pool.k[:0], step.pool.v[:0])  # a pool of no blocks
+    with pytest.raises(pa.PaError) as e:
+        pa.forward(step.q, step.out, step.qsl, step.seq, w.qsl, w.seq_lens, step.gathered,
+                   empty, w.scale, 1)
+    assert e.value.status == pa.PA_ERR_INVALID
