@@ -324,6 +324,25 @@ def timed_flushed(fn, steps, warmup, stream):
     return sum(a.elapsed_time(b) for a, b in ev) / steps
 
 
+def run_decode(args, dev):
+    """The decode batch of the benchmark line alone, one whole step (staged
+    diffs, KV write, forward) per iteration: a narrow command for profiler
+    captures (no e2e leg, no secondary workloads, no clock sampling)."""
+    import torch
+
+    import workloads
+    from paged_kv_cache_143_gb300 import accounting, pa
+
+    w = workloads.make(CONFIG_ID, device=dev, num_requests=args.requests)
+    kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    step = Step(w, dev, max_splits=32)
+    ms = timed(step.run, args.steps, args.warmup, torch.cuda.current_stream())
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the decode batch")
+    return {"workload": f"decode-7b-like: {w.R} requests x 1 token", "kv_bytes": kv,
+            "ms_per_step": round(ms, 5), "gbs": round(kv / (ms * 1e-3) / 1e9, 1)}
+
+
 def run_mixed(args, dev, cfg, kv_dtype=None):
     """Mixed decode + prefill step of config `cfg` (tokens/s of the whole step),
     and the prefill kernel alone on the same chunks (causal TFLOP/s)."""
@@ -670,18 +689,20 @@ def main():
     ap.add_argument("--requests", type=int, default=256,
                     help="decode batch size (256 is the benchmark workload; smaller sizes "
                          "are for profiling captures)")
-    ap.add_argument("--only", choices=["mixed", "long-bf16", "long-fp8", "prefix-shared", "tiny",
-                                       "serving"],
+    ap.add_argument("--only", choices=["decode", "mixed", "long-bf16", "long-fp8",
+                                       "prefix-shared", "tiny", "serving"],
                     default=None,
-                    help="run one secondary workload alone and print its object (a narrow "
-                         "command for profiler captures; not the benchmark line)")
+                    help="run one workload alone (the benchmark's decode batch or a "
+                         "secondary workload) and print its object (a narrow command for "
+                         "profiler captures; not the benchmark line)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.only:
         import torch
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)
-        run = {"mixed": lambda: run_mixed(args, dev, 3),
+        run = {"decode": lambda: run_decode(args, dev),
+               "mixed": lambda: run_mixed(args, dev, 3),
                "long-bf16": lambda: run_mixed(args, dev, 5, "bf16"),
                "long-fp8": lambda: run_mixed(args, dev, 5, "fp8"),
                "prefix-shared": lambda: run_prefix_shared(args, dev),
