@@ -87,3 +87,69 @@ def test_shared_prefix_host_rejections():
     assert call(qsl, seq, i32(0), i32(2), i32(2), ws_bytes=0) == pa.PA_ERR_INVALID
     one_split = pa.forward_workspace_size(3, 4, 64, 1)
     assert call(qsl, seq, i32(0), i32(2), i32(2), ws_bytes=one_split) == pa.PA_ERR_INVALID
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "pa.h"
+#include "pa_sched.h"
+
+static const void* const every_entry_point[] = {
+%s
+};
+
+int main(void) {
+  size_t i, n = sizeof every_entry_point / sizeof every_entry_point[0];
+  for (i = 0; i < n; ++i)
+    if (!every_entry_point[i]) return 2;
+  pa_sched_config cfg = {64, 16, 8, 16, 256, 128, 1};
+  pa_sched* s = NULL;
+  if (pa_sched_create(&cfg, &s) != PA_OK) return 3;
+  int32_t prompt[40];
+  for (i = 0; i < 40; ++i) prompt[i] = (int32_t)i;
+  if (pa_sched_add_request(s, 7, prompt, 40, 2, 0) != PA_OK) return 4;
+  pa_sched_batch b;
+  if (pa_sched_step(s, &b) != PA_OK) return 5;
+  printf("%%d %%d %%d %%lld\n", b.num_reqs, b.num_tokens, b.num_decode, (long long)b.req_ids[0]);
+  int32_t sampled[1] = {99}, num_finished = 0;
+  if (pa_sched_commit(s, sampled, b.num_reqs, NULL, 0, &num_finished) != PA_OK) return 6;
+  if (pa_sched_step(s, &b) != PA_OK) return 7;
+  printf("%%d %%d %%d %%d\n", b.num_reqs, b.num_tokens, b.num_decode, b.positions[0]);
+  printf("%%s\n", pa_status_string(PA_ERR_INVALID));
+  pa_sched_destroy(s);
+  return 0;
+}
+"""
+
+
+def _compile_and_link(tmp_path, compiler, flags, suffix):
+    import shutil
+    import subprocess
+    if shutil.which(compiler) is None:
+        import pytest
+        pytest.skip(f"{compiler} not available")
+    lib_dir = os.path.dirname(pa.lib()._name)
+    src = tmp_path / f"use_pa.{suffix}"
+    refs = ",\n".join(f"    (const void*)&{name}" for name in declared_functions())
+    src.write_text(C_PROGRAM % refs)
+    exe = tmp_path / f"use_pa_{suffix}"
+    r = subprocess.run([compiler, *flags, "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", lib_dir, "-lpa", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    return exe
+
+
+def test_headers_build_a_plain_c_program_that_drives_the_scheduler(tmp_path):
+    """Both headers compile as C99 and as C++17 against the library, every
+    declared entry point links, and the host-only scheduler runs from C:
+    a 40-token prompt is one 40-token chunk, then one decode at position 40."""
+    import subprocess
+    exe = _compile_and_link(tmp_path, "gcc", ["-std=c99"], "c")
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    lines = r.stdout.splitlines()
+    assert lines[0] == "1 40 0 7"
+    assert lines[1] == "1 1 1 40"
+    assert lines[2] == pa.status_string(pa.PA_ERR_INVALID)
+    _compile_and_link(tmp_path, "g++", ["-std=c++17"], "cpp")
