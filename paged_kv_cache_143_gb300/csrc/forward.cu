@@ -61,6 +61,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   if (cas && cas->n > 0 && (!cas->first_host || !cas->size_host || !cas->prefix_blocks_host))
     return PA_ERR_INVALID;
   if (R == 0) return T == 0 && (!cas || cas->n == 0) ? PA_OK : PA_ERR_INVALID;
+  if (T > 0 && pool->num_blocks == 0) return PA_ERR_INVALID;  // no block a table could name
   if (!qsl_host || !seq_lens_host || !query_start_loc || !seq_lens || !block_tables)
     return PA_ERR_INVALID;
   if (T > 0 && (!q || !out || !pa::aligned16(q) || !pa::aligned16(out))) return PA_ERR_INVALID;
@@ -176,7 +177,6 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   };
 
   if (n_dec > 0) {
-    if (pool->num_blocks == 0) return PA_ERR_INVALID;  // no block a table could name
     pa::DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.out = static_cast<__nv_bfloat16*>(out);
@@ -282,7 +282,6 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
                        [&](int a, int b) { return work(a) > work(b); });
       L.p.n_order = n;
     }
-    if (pool->num_blocks == 0) return PA_ERR_INVALID;
     if (pa::launch_prefill(L, s) != cudaSuccess) return PA_ERR_CUDA;
     pa::count_launches(1);
   }

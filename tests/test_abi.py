@@ -48,6 +48,14 @@ def test_status_strings_and_host_side_rejections():
     assert L.pa_write_kv(ctypes.byref(fp8), None, None, None, 0, None) == pa.PA_ERR_INVALID
     mis = pa._Pool(17, 16, 4, 16, 1, 64, 0, 1.0, 1.0)  # misaligned pool
     assert L.pa_write_kv(ctypes.byref(mis), None, None, None, 0, None) == pa.PA_ERR_INVALID
+    # a pool of no blocks cannot hold any request's keys (fake, aligned device
+    # pointers: the call returns before touching them)
+    import numpy as np
+    empty = pa._Pool(16, 16, 0, 16, 1, 64, 0, 1.0, 1.0)
+    qsl, seq = np.array([0, 1], np.int32), np.array([5], np.int32)
+    assert L.pa_forward(16, 16, 16, 16, qsl.ctypes.data_as(ctypes.c_void_p),
+                        seq.ctypes.data_as(ctypes.c_void_p), 16, 1, 1, 1, 1,
+                        ctypes.byref(empty), 0.125, 1, None, 0, None) == pa.PA_ERR_INVALID
 
 
 def test_workspace_size_formula():
