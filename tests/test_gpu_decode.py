@@ -51,6 +51,7 @@ CASES = [
     ([17, 1111], 4, 1, 64, 32, "bf16"),                 # g = 4, D = 64
     ([3, 47, 1500], 32, 2, 128, 16, "fp8"),             # g = 16: hi and mid in two products
     ([11, 260, 33], 8, 4, 64, 32, "fp8"),               # g = 2, D = 64
+    ([31, 32, 33, 777], 16, 8, 128, 32, "fp8"),         # g = 2, B = 32: two chunks per block
 ]
 
 
