@@ -409,19 +409,24 @@ class SchedBatch:
     FIELDS = ("req_ids", "idx_mapping", "num_scheduled", "query_start_loc", "seq_lens",
               "positions", "token_ids", "slot_mapping", "diff_rows", "diff_starts",
               "diff_val_offsets", "diff_vals", "copy_src", "copy_dst")
+    _INT64 = frozenset(("req_ids", "slot_mapping"))
 
     def __init__(self, b: "_SchedBatch"):
         R, T, W, C = b.num_reqs, b.num_tokens, b.num_diffs, b.num_copies
         n_vals = b.diff_val_offsets[W] if W >= 0 else 0
-        sizes = dict(req_ids=R, idx_mapping=R, num_scheduled=R, query_start_loc=R + 1,
-                     seq_lens=R, positions=T, token_ids=T, slot_mapping=T, diff_rows=W,
-                     diff_starts=W, diff_val_offsets=W + 1, diff_vals=n_vals, copy_src=C,
-                     copy_dst=C)
-        for name in self.FIELDS:
-            ptr, n = getattr(b, name), sizes[name]
-            dt = np.int64 if name in ("req_ids", "slot_mapping") else np.int32
-            setattr(self, name, np.ctypeslib.as_array(ptr, shape=(n,)).astype(dt, copy=True)
-                    if n > 0 else np.zeros(0, dt))
+        sizes = (R, R, R, R + 1, R, T, T, T, W, W, W + 1, n_vals, C, C)
+        # one memcpy per field (string_at) into a writable buffer: the
+        # per-call cost of np.ctypeslib.as_array dominated a serving step's
+        # host time
+        for name, n in zip(self.FIELDS, sizes):
+            dt = np.int64 if name in self._INT64 else np.int32
+            if n > 0:
+                addr = ctypes.cast(getattr(b, name), ctypes.c_void_p).value
+                nbytes = n * (8 if dt is np.int64 else 4)
+                arr = np.frombuffer(bytearray(ctypes.string_at(addr, nbytes)), dt)
+            else:
+                arr = np.zeros(0, dt)
+            setattr(self, name, arr)
         self.num_decode = b.num_decode
 
     @property
