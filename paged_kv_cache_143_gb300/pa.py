@@ -190,6 +190,11 @@ def _dptr(t: Optional[torch.Tensor], dtype=None) -> Optional[int]:
     return t.data_ptr() if t.numel() else None
 
 
+def _np_addr(a: np.ndarray) -> int:
+    """Address of a contiguous numpy array's data (cheaper than .ctypes)."""
+    return a.__array_interface__["data"][0]
+
+
 def _host_i32(a) -> np.ndarray:
     if isinstance(a, torch.Tensor):
         a = a.detach().cpu().numpy()
@@ -453,7 +458,7 @@ class Scheduler:
 
     def add_request(self, req_id: int, prompt, max_new: int, salt: int = 0) -> None:
         p = np.ascontiguousarray(prompt, dtype=np.int32)
-        _check(lib().pa_sched_add_request(self._h, int(req_id), p.ctypes.data_as(ctypes.c_void_p),
+        _check(lib().pa_sched_add_request(self._h, int(req_id), _np_addr(p),
                                           p.size, int(max_new), int(salt) & (2**64 - 1)),
                "pa_sched_add_request")
 
@@ -473,8 +478,7 @@ class Scheduler:
         s = np.ascontiguousarray(sampled, dtype=np.int32)
         ids = np.zeros(max(s.size, 1), np.int64)
         n = ctypes.c_int32()
-        _check(lib().pa_sched_commit(self._h, s.ctypes.data_as(ctypes.c_void_p), s.size,
-                                     ids.ctypes.data_as(ctypes.c_void_p), ids.size,
+        _check(lib().pa_sched_commit(self._h, _np_addr(s), s.size, _np_addr(ids), ids.size,
                                      ctypes.byref(n)), "pa_sched_commit")
         return ids[:n.value].tolist()
 
