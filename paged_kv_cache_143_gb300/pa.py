@@ -223,11 +223,25 @@ class KVPool:
         return _Pool(_dptr(self.k), _dptr(self.v), self.num_blocks, self.block_size,
                      self.num_kv_heads, self.head_dim, self.dtype, self.k_scale, self.v_scale)
 
+    def ref(self):
+        """ctypes reference to the pool's C struct, built once and rebuilt
+        after any attribute is reassigned."""
+        c = self.__dict__.get("_c")
+        if c is None:
+            st = self.struct()
+            c = (st, ctypes.byref(st))
+            self.__dict__["_c"] = c
+        return c[1]
+
+    def __setattr__(self, name, value):
+        self.__dict__.pop("_c", None)
+        object.__setattr__(self, name, value)
+
 
 def write_kv(pool: KVPool, k_new: torch.Tensor, v_new: torch.Tensor,
              slot_mapping: torch.Tensor, stream=None) -> None:
     T = slot_mapping.numel()
-    st = lib().pa_write_kv(ctypes.byref(pool.struct()), _dptr(k_new, torch.bfloat16),
+    st = lib().pa_write_kv(pool.ref(), _dptr(k_new, torch.bfloat16),
                            _dptr(v_new, torch.bfloat16), _dptr(slot_mapping, torch.int64), T,
                            _stream(stream))
     _check(st, "pa_write_kv")
@@ -253,9 +267,9 @@ def forward(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.Tensor,
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().pa_forward(
         _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
-        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
-        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
-        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), ws_ptr, ws_bytes,
+        _dptr(seq_lens, torch.int32), _np_addr(qh),
+        _np_addr(sh), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, pool.ref(), float(scale), int(causal), ws_ptr, ws_bytes,
         _stream(stream))
     _check(st, "pa_forward")
 
@@ -288,12 +302,12 @@ def forward_shared_prefix(q: torch.Tensor, out: torch.Tensor, query_start_loc: t
     max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
     ws_ptr = _dptr(workspace) if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    host = lambda a: a.ctypes.data_as(ctypes.c_void_p) if G > 0 else None
+    host = lambda a: _np_addr(a) if G > 0 else None
     st = lib().pa_forward_shared_prefix(
         _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
-        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
-        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
-        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), G, host(gf), host(gn),
+        _dptr(seq_lens, torch.int32), _np_addr(qh),
+        _np_addr(sh), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, pool.ref(), float(scale), int(causal), G, host(gf), host(gn),
         host(pb), ws_ptr, ws_bytes, _stream(stream))
     _check(st, "pa_forward_shared_prefix")
 
@@ -318,9 +332,9 @@ def forward_noalloc(q: torch.Tensor, out: torch.Tensor, query_start_loc: torch.T
     max_blocks = block_tables.shape[1] if block_tables.dim() == 2 else 0
     st = lib().pa_forward_noalloc(
         _dptr(q, torch.bfloat16), _dptr(out, torch.bfloat16), _dptr(query_start_loc, torch.int32),
-        _dptr(seq_lens, torch.int32), qh.ctypes.data_as(ctypes.c_void_p),
-        sh.ctypes.data_as(ctypes.c_void_p), _dptr(block_tables, torch.int32), max_blocks, R, T,
-        Hq, ctypes.byref(pool.struct()), float(scale), int(causal), int(max_splits),
+        _dptr(seq_lens, torch.int32), _np_addr(qh),
+        _np_addr(sh), _dptr(block_tables, torch.int32), max_blocks, R, T,
+        Hq, pool.ref(), float(scale), int(causal), int(max_splits),
         _stream(stream))
     _check(st, "pa_forward_noalloc")
 
@@ -523,7 +537,7 @@ def apply_staged_writes(table: torch.Tensor, rows: torch.Tensor, starts: torch.T
 
 
 def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
-    st = lib().pa_copy_blocks(ctypes.byref(pool.struct()), _dptr(src, torch.int32),
+    st = lib().pa_copy_blocks(pool.ref(), _dptr(src, torch.int32),
                               _dptr(dst, torch.int32), src.numel(), _stream(stream))
     _check(st, "pa_copy_blocks")
 
