@@ -161,3 +161,26 @@ def test_headers_build_a_plain_c_program_that_drives_the_scheduler(tmp_path):
     assert lines[1] == "1 1 1 40"
     assert lines[2] == pa.status_string(pa.PA_ERR_INVALID)
     _compile_and_link(tmp_path, "g++", ["-std=c++17"], "cpp")
+
+
+def test_pool_struct_is_cached_and_rebuilt_on_reassignment(monkeypatch):
+    """KVPool.ref() hands the C ABI one struct per pool; reassigning a scale
+    or a tensor rebuilds it (CPU tensors stand in for device ones: only
+    their addresses are read)."""
+    import torch
+    monkeypatch.setattr(pa, "_dptr", lambda t, dtype=None: t.data_ptr() if t.numel() else None)
+    k = torch.zeros(8, 2, 16, 64, dtype=torch.uint8)
+    v = torch.zeros_like(k)
+    pool = pa.KVPool(k, v, 0.5, 0.25)
+    read = lambda r: ctypes.cast(r, ctypes.POINTER(pa._Pool)).contents
+    r = pool.ref()
+    s = read(r)
+    assert (s.k_pool, s.v_pool) == (k.data_ptr(), v.data_ptr())
+    assert (s.num_blocks, s.num_kv_heads, s.block_size, s.head_dim) == (8, 2, 16, 64)
+    assert (s.dtype, s.k_scale, s.v_scale) == (pa.PA_KV_FP8_E4M3, 0.5, 0.25)
+    assert pool.ref() is r
+    pool.k_scale = 2.0
+    assert pool.ref() is not r and read(pool.ref()).k_scale == 2.0
+    k2 = torch.zeros_like(k)
+    pool.k = k2
+    assert read(pool.ref()).k_pool == k2.data_ptr()
