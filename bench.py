@@ -9,8 +9,14 @@ job over all GPUs (replicas: every rank runs its own batch).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl libpa|reference]
 
---impl reference times the CPU oracle (fp64, all host cores) on a bounded
-sample of the same workload and prints the same line with "impl": "reference".
+--impl reference times the CPU oracle (fp64, all host cores) on the same
+256-request step and prints the same line with "impl": "reference". The GPU
+line also carries, for the headline batch and for every secondary workload
+(tiny decode, mixed chunked prefill, long context bf16 / E4M3, prefix-shared
+sampling), the oracle's time for that workload's whole step on the host
+cores: measured whole where that takes about ten seconds or less, else
+measured on a stated uniform sample of output rows and scaled by visible
+(row, key) pairs (oracle_baseline).
 """
 import argparse
 import hashlib
@@ -247,6 +253,9 @@ def run_libpa(args):
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside
     e2e = run_e2e(args, w, step, dev, kv_bytes, world)
+    # the oracle beside it, on the host cores (rank 0 of a one-GPU run only)
+    args.cpu_legs = args.cpu_legs and world == 1 and rank == 0
+    cpu = cpu_baseline(w, kv_bytes) if args.cpu_legs else None
 
     peak, peak_kind = load_peaks()
     achieved = total_kv / world / (fwd_ms * 1e-3) / 1e9  # per GPU
@@ -282,7 +291,8 @@ def run_libpa(args):
     line["tiny_decode"] = run_tiny(args, dev)
     line["serving"] = run_serving(args, dev)
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(args)
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -383,7 +393,11 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
     tf = flops / (ms_pre * 1e-3) / 1e12
     del step, sp, sd
     torch.cuda.empty_cache()
-    return {
+    cpu = None
+    if getattr(args, "cpu_legs", False):
+        cpu = oracle_baseline(w, seed=cfg)
+        cpu.update({"value": round(w.T / cpu["seconds_per_step"], 2), "unit": "tokens/s"})
+    return {"cpu_baseline": cpu,
         "workload": w.name, "tokens_per_step": int(w.T), "ms_per_step": round(ms, 4),
         "tokens_per_s": round(w.T / (ms * 1e-3), 1),
         "step": "pa_apply_staged_writes + pa_write_kv + pa_forward (decodes and chunks)",
@@ -426,6 +440,11 @@ def run_prefix_shared(args, dev):
                     "unique_frac_of_hbm": round(unique / (ms_fwd * 1e-3) / 1e9 / peak, 4)}
     del step
     torch.cuda.empty_cache()
+    if getattr(args, "cpu_legs", False):
+        cpu = oracle_baseline(w, seed=4)
+        cpu.update({"value": round(logical / cpu["seconds_per_step"] / 1e9, 4),
+                    "unit": "GB/s (logical KV bytes)"})
+        res["cpu_baseline"] = cpu
     return res
 
 
@@ -464,7 +483,11 @@ def run_tiny(args, dev, graph_steps=8):
         raise RuntimeError("device error in the tiny decode runs")
     kernels = g.kernels
     g.close()
-    return {"workload": w.name, "us_per_step": round(us, 2),
+    cpu = None
+    if getattr(args, "cpu_legs", False):
+        cpu = oracle_baseline(w, budget_s=2.0, seed=1)
+        cpu.update({"value": round(cpu["seconds_per_step"] * 1e6, 2), "unit": "us per step"})
+    return {"workload": w.name, "us_per_step": round(us, 2), "cpu_baseline": cpu,
             "graph": {"steps_per_launch": N, "us_per_step": round(us_graph, 2),
                       "kernels_per_launch": kernels,
                       "step": "pa_prepare_inputs + pa_write_kv + pa_forward, captured"}}
@@ -612,41 +635,99 @@ def run_e2e(args, w, step, dev, kv_bytes, world):
 
 # ------------------------------------------------------------- oracle arms
 
-SAMPLE_REQUESTS = 64
-CPU_SAMPLE_SECONDS = 10.0
+CPU_SAMPLE_SECONDS = 10.0  # oracle seconds per workload (about; whole configs may take less)
 
 
-def oracle_sample_step(w):
-    """One step of the oracle on a sample workload: staged diffs + gather, KV
-    write, attention. Returns seconds."""
+def visible_pairs(w):
+    """Visible (query row, key) pairs of every output row, token-major
+    [T * Hq]: the oracle's work per row is proportional to them."""
+    per_tok = np.zeros(int(w.T), np.int64)
+    for r in range(w.R):
+        a, b = int(w.qsl[r]), int(w.qsl[r + 1])
+        if b == a:
+            continue
+        seq = int(w.seq_lens[r])
+        P = seq - (b - a)
+        per_tok[a:b] = P + 1 + np.arange(b - a) if (w.causal and b - a > 1) else seq
+    return np.repeat(per_tok, w.Hq)
+
+
+class OracleStep:
+    """The oracle's copy of one step's inputs (prepared outside any timing)
+    and one timed pass: staged diffs + gather, KV write, attention over all
+    output rows or a subset."""
+
+    def __init__(self, w):
+        from tests.helpers import bits, oracle_pool
+        self.w = w
+        self.pool = oracle_pool(w, include_new=False)
+        self.k_new, self.v_new = bits(w.new_k), bits(w.new_v)
+        self.slots, self.q = w.slot_mapping.cpu().numpy(), bits(w.q)
+
+    def run(self, rows=None):
+        from oracle import oracle as O
+        w = self.w
+        table = w.table_before.copy()
+        t = time.perf_counter()
+        gathered = O.apply_staged_writes(table, w.diff_rows, w.diff_starts, w.diff_val_offsets,
+                                         w.diff_vals, w.idx_mapping)
+        O.write_kv(self.pool, self.k_new, self.v_new, self.slots)
+        O.paged_attention(self.q, w.qsl, w.seq_lens, gathered, self.pool, w.scale, w.causal,
+                          rows=rows)
+        return time.perf_counter() - t
+
+
+def oracle_baseline(w, budget_s=CPU_SAMPLE_SECONDS, seed=0):
+    """Times the fp64 C oracle on the host cores on workload `w`: the whole
+    step if it fits in about `budget_s` seconds, else a uniform random sample
+    of output rows (token, head) sized to the budget. For a sample, the step's
+    fixed part (staged diffs + KV write, timed with a one-row attention) is
+    kept and the attention part is scaled by visible (row, key) pairs, to
+    which the oracle's work per row is proportional. Returns the seconds of
+    one whole step and a description of what ran."""
     from oracle import oracle as O
-    from tests.helpers import bits, oracle_pool
-    pool = oracle_pool(w, include_new=False)
-    k_new, v_new, slots, q = bits(w.new_k), bits(w.new_v), w.slot_mapping.numpy(), bits(w.q)
-    t = time.perf_counter()
-    table = w.table_before.copy()
-    gathered = O.apply_staged_writes(table, w.diff_rows, w.diff_starts, w.diff_val_offsets,
-                                     w.diff_vals, w.idx_mapping)
-    O.write_kv(pool, k_new, v_new, slots)
-    O.paged_attention(q, w.qsl, w.seq_lens, gathered, pool, w.scale, w.causal)
-    return time.perf_counter() - t
-
-
-def cpu_baseline(args, n_req=SAMPLE_REQUESTS):
-    import workloads
-    from oracle import oracle as O
-    from paged_kv_cache_143_gb300 import accounting
-    w = workloads.make(CONFIG_ID, device="cpu", sub=9, num_requests=n_req)
-    kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    st = OracleStep(w)
+    pairs = visible_pairs(w)
+    total = int(pairs.sum())
+    rng = np.random.default_rng(143000 + seed)
+    one = np.zeros(1, np.int64)
+    t_fixed = min(st.run(one) for _ in range(3))
+    # calibration: about two million pairs' worth of rows
+    n_cal = int(min(pairs.size, max(64, 2_000_000 * pairs.size // max(total, 1))))
+    cal = np.sort(rng.choice(pairs.size, size=n_cal, replace=False)) if n_cal < pairs.size else None
+    t_cal = st.run(cal)
+    cal_pairs = int(pairs[cal].sum()) if cal is not None else total
+    rate = cal_pairs / max(t_cal - t_fixed, 1e-9)  # attention pairs per second
+    frac = min(1.0, max(budget_s - t_fixed, 0.1) * rate / max(total, 1))
+    if frac >= 0.999 or cal is None:
+        rows, sample_pairs = None, total
+    else:
+        n = max(1, int(pairs.size * frac))
+        rows = np.sort(rng.choice(pairs.size, size=n, replace=False))
+        sample_pairs = int(pairs[rows].sum())
     secs = []
-    while not secs or sum(secs) < CPU_SAMPLE_SECONDS:
-        secs.append(oracle_sample_step(w))
-    s = sum(secs) / len(secs)
-    return {"value": round(kv / s / 1e9, 4), "unit": UNIT, "cores": O.max_threads(),
-            "kind": "oracle", "seconds_per_step": round(s, 4), "steps": len(secs),
-            "sample": f"{len(secs)} steps of a {n_req}-request batch of the same decode "
-                      f"workload ({int(w.seq_lens.sum())} keys, {kv} KV bytes per step), "
-                      f"fp64 C oracle"}
+    while not secs or (rows is None and sum(secs) < budget_s and len(secs) < 50):
+        secs.append(st.run(rows))
+    s_sample = sum(secs) / len(secs)
+    if rows is None:
+        whole = s_sample
+        what = f"the whole step, {len(secs)} run(s)"
+    else:
+        whole = t_fixed + max(s_sample - t_fixed, 0.0) * total / sample_pairs
+        what = (f"{rows.size} of {pairs.size} output rows (token x head) drawn uniformly, "
+                f"{sample_pairs} of {total} visible (row, key) pairs; whole-step time = "
+                f"fixed part ({t_fixed:.4f} s: diffs, KV write) + attention part scaled by "
+                f"pairs")
+    return {"seconds_per_step": round(whole, 5), "measured_seconds": round(s_sample, 5),
+            "sampled": rows is not None, "cores": O.max_threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle (staged diffs + KV write + attention) on {what}"}
+
+
+def cpu_baseline(w, kv_bytes):
+    """The oracle beside the headline decode batch: KV GB/s of the whole step."""
+    b = oracle_baseline(w)
+    b.update({"value": round(kv_bytes / b["seconds_per_step"] / 1e9, 4), "unit": UNIT})
+    return b
 
 
 def run_reference(args):
@@ -656,12 +737,12 @@ def run_reference(args):
     import workloads
     from oracle import oracle as O
     from paged_kv_cache_143_gb300 import accounting
-    n_req = SAMPLE_REQUESTS
-    w = workloads.make(CONFIG_ID, device="cpu", sub=9, num_requests=n_req)
+    w = workloads.make(CONFIG_ID, device="cpu", num_requests=args.requests)
     kv = accounting.decode_kv_bytes(w.seq_lens, w.Hkv, w.D, w.elt_bytes)
+    st = OracleStep(w)
     for _ in range(args.warmup):
-        oracle_sample_step(w)
-    secs = [oracle_sample_step(w) for _ in range(args.steps)]
+        st.run()
+    secs = [st.run() for _ in range(args.steps)]
     s = sum(secs) / len(secs)
     value = round(kv / s / 1e9, 4)
     line = {
@@ -669,12 +750,14 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": f"decode-7b-like sample: {n_req} requests x 1 token, 32/32 heads, "
-                               f"head_dim 128, block 16, contexts U[128,2048]",
-                   "kv_bytes_per_step": kv},
+        "config": {"workload": f"decode-7b-like: {w.R} requests x 1 token, 32/32 heads, "
+                               f"head_dim 128, block 16, contexts U[128,2048] "
+                               f"({int(w.seq_lens.sum())} keys), bf16 KV",
+                   "kv_bytes_per_step": kv,
+                   "step": "staged diffs + KV write + attention, fp64 C oracle"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.max_threads(),
                          "kind": "oracle",
-                         "sample": f"{n_req}-request sample of the decode workload per step"},
+                         "sample": f"the whole {w.R}-request step, {args.steps} timed steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -689,6 +772,8 @@ def main():
     ap.add_argument("--requests", type=int, default=256,
                     help="decode batch size (256 is the benchmark workload; smaller sizes "
                          "are for profiling captures)")
+    ap.add_argument("--no-cpu", dest="cpu_legs", action="store_false",
+                    help="skip the oracle timings on the host cores (profiling runs)")
     ap.add_argument("--only", choices=["decode", "mixed", "long-bf16", "long-fp8",
                                        "prefix-shared", "tiny", "serving"],
                     default=None,
@@ -698,6 +783,7 @@ def main():
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.only:
+        args.cpu_legs = False
         import torch
         dev = torch.device("cuda", 0)
         torch.cuda.set_device(dev)

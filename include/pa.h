@@ -28,6 +28,11 @@
  *    error are unspecified.
  *  - All pointers marked "dev" are device pointers on the current device; "host"
  *    pointers are read synchronously during the call only.
+ *  - The library looks up the device addresses of its own device variables
+ *    (the error word, the scratch array of pa_forward_noalloc) once per device,
+ *    on first use, and keeps them for the life of the process. They do not
+ *    survive cudaDeviceReset: after a reset of a device, make no further call
+ *    of this library on that device in the same process.
  */
 #ifndef PA_H
 #define PA_H
@@ -153,6 +158,11 @@ size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_heads, int32_t 
  * 1 <= q_len <= seq_len <= max_blocks * block_size for every request with
  * q_len > 0, and a pool with at least one block when any request has
  * q_len > 0; otherwise PA_ERR_INVALID.
+ * Device checks: the grids are planned from the host mirrors. A device
+ * query_start_loc or seq_lens that disagrees with them so that a request's
+ * rows would leave [0, T), or its keys or query tiles would need more CTAs
+ * or workspace slots than were planned, sets PA_ERR_DEVICE_BOUNDS; nothing is
+ * read or written outside q, out, the pool and the workspace.
  */
 pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
                      const int32_t* seq_lens, const int32_t* qsl_host,
@@ -370,6 +380,10 @@ pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32
  * device error word of the current device: PA_ERR_TIMEOUT if a bounded wait
  * gave up, else PA_ERR_DEVICE_BOUNDS if an index was out of range, else
  * PA_OK. Returns PA_ERR_CUDA if the synchronisation itself failed.
+ * The word is read and cleared in one atomic exchange (a one-thread kernel on
+ * `stream`, counted by pa_kernel_launches), so a bit that a kernel on another
+ * stream sets meanwhile is returned by this call or by the next one, never
+ * cleared unseen. Not callable during stream capture (it synchronises).
  */
 pa_status pa_get_error(pa_stream_t stream);
 
@@ -397,7 +411,8 @@ const char* pa_status_string(pa_status status);
  *
  * The call allocates nothing and frees nothing. The first call on each device
  * looks up the array's device address (cudaGetSymbolAddress) and caches it;
- * make that first call before any stream capture. Every call shares the same
+ * make that first call before any stream capture. The cached address does not
+ * survive cudaDeviceReset (see the conventions above). Every call shares the same
  * array: calls that may run at the same time on the GPU (different streams,
  * or several host threads) race on it and must be serialised by the caller.
  * The array keeps the previous call's contents; nothing needs clearing,

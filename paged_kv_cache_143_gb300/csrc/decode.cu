@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
   const int r = blockIdx.z;
   const int qs = p.qsl[r];
   if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
+  if (qs < 0 || qs >= p.T) {  // a device qsl that leaves q / out
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
   const int seq = p.seq_lens[r];
   if (seq < 1 || seq > p.max_blocks * p.B) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
@@ -464,6 +468,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int r = blockIdx.z;
   const int qs = p.qsl[r];
   if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
+  if (qs < 0 || qs >= p.T) {  // a device qsl that leaves q / out
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
   const int seq = p.seq_lens[r];
   if (seq < 1 || seq > p.max_blocks * p.B) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
@@ -802,7 +810,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeParams p)
   const int h = blockIdx.x * kMergeWarps + (threadIdx.x >> 5), r = blockIdx.y;
   if (h >= p.Hq) return;
   const int qs = p.qsl[r], qe = p.qsl[r + 1], seq = p.seq_lens[r];
-  if (qe - qs != 1) return;
+  if (qe - qs != 1 || qs < 0 || qs >= p.T) return;  // the decode kernel flagged a bad qsl
   if (seq < 1 || seq > p.max_blocks * p.B) return;
   const int grp_id = group_of(p.groups, r);
   const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;

@@ -153,6 +153,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   auto prefill_launch = [&]() {
     pa::PrefillLaunch L{};
     L.p.out = static_cast<__nv_bfloat16*>(out);
+    L.p.T = T;
     L.p.qsl = query_start_loc;
     L.p.seq_lens = seq_lens;
     L.p.block_tables = block_tables;
@@ -180,6 +181,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     pa::DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.out = static_cast<__nv_bfloat16*>(out);
+    p.T = T;
     p.qsl = query_start_loc;
     p.seq_lens = seq_lens;
     p.block_tables = block_tables;

@@ -12,7 +12,9 @@
 // library holds PA_NOALLOC_SCRATCH_BYTES of it until the process exits. Host
 // code cannot use the symbol as a pointer (on the host it only names a
 // stand-in), so its device address is looked up once per device with
-// cudaGetSymbolAddress and cached.
+// cudaGetSymbolAddress and cached. The cache is never invalidated: after
+// cudaDeviceReset the address is stale, and the library must not be called
+// on that device again in the same process.
 #include <mutex>
 
 #include "pa_internal.h"

@@ -7,6 +7,7 @@
 
 namespace {
 __device__ unsigned g_error_word;  // sticky bits: pa::kErrBounds | pa::kErrTimeout
+__device__ unsigned g_error_taken;  // where pa_get_error's exchange leaves the bits
 
 constexpr int kMaxDevices = 64;
 unsigned* g_word_addr[kMaxDevices];
@@ -83,13 +84,32 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace pa
 
+namespace {
+// Reads and clears the error word in one atomic exchange, so that a bit set
+// by a kernel on another stream is either returned now or kept for the next
+// call, never cleared unseen.
+__global__ void take_error_kernel(unsigned* word, unsigned* taken) {
+  *taken = atomicExch(word, 0u);
+}
+std::mutex g_take_mu;  // one taker at a time per process (they share g_error_taken)
+}  // namespace
+
 extern "C" pa_status pa_get_error(pa_stream_t stream) {
-  if (cudaStreamSynchronize(pa::as_stream(stream)) != cudaSuccess) return PA_ERR_CUDA;
+  cudaStream_t s = pa::as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
   unsigned* w = pa::error_word();
   if (!w) return PA_ERR_CUDA;
   unsigned bits = 0;
-  if (cudaMemcpy(&bits, w, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
-  if (bits && cudaMemset(w, 0, sizeof bits) != cudaSuccess) return PA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_take_mu);
+    void* taken = nullptr;
+    if (cudaGetSymbolAddress(&taken, g_error_taken) != cudaSuccess) return PA_ERR_CUDA;
+    take_error_kernel<<<1, 1, 0, s>>>(w, static_cast<unsigned*>(taken));
+    if (pa::launch_status() != PA_OK) return PA_ERR_CUDA;
+    if (cudaMemcpyAsync(&bits, taken, sizeof bits, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
   if (bits & 2u) return PA_ERR_TIMEOUT;
   if (bits & 1u) return PA_ERR_DEVICE_BOUNDS;
   return PA_OK;

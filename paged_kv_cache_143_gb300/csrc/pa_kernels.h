@@ -40,6 +40,7 @@ __host__ __device__ inline int prefix_slots(const GroupDesc& gd, int grp) {
 struct DecodeParams {
   const __nv_bfloat16* q;      // [T][Hq][D]
   __nv_bfloat16* out;          // [T][Hq][D]
+  int32_t T;                   // rows of q and out: every device qsl entry must be <= T
   const int32_t* qsl;          // [R+1]
   const int32_t* seq_lens;     // [R]
   const int32_t* block_tables; // [R][max_blocks]
@@ -65,6 +66,7 @@ constexpr int kMaxOrderedPrefill = 256;
 
 struct PrefillParams {
   __nv_bfloat16* out;          // [T][Hq][D]
+  int32_t T;                   // rows of q and out: every device qsl entry must be <= T
   const int32_t* qsl;          // [R+1]
   const int32_t* seq_lens;     // [R]
   const int32_t* block_tables; // [R][max_blocks]

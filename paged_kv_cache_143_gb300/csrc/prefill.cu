@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     r = p.groups.first[grp];
     q_begin = p.qsl[r];
     q_len = p.groups.size[grp];
-    if (p.qsl[r + q_len] - q_begin != q_len) {  // members are not all decodes
+    if (p.qsl[r + q_len] - q_begin != q_len || q_begin < 0 || q_begin + q_len > p.T) {
+      // members are not all decodes, or a device qsl leaves q
       if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
       return;
     }
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     q_len = p.qsl[r + 1] - q_begin;
     if (q_len <= 1) return;  // decode requests and empty requests are not ours
     seq = p.seq_lens[r];
-    if (seq < q_len || seq > p.max_blocks * p.B) {
+    if (seq < q_len || seq > p.max_blocks * p.B || q_begin < 0 || q_begin + q_len > p.T) {
       if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
       return;
     }
@@ -193,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tpt = kM / g;  // tokens per tile
   const int ntq = (q_len + tpt - 1) / tpt;
   const int npairs = (ntq + 1) / 2;
+  if (npairs > (p.mode == 1 ? p.pairs_per_piece : (int)gridDim.x)) {
+    // more query tiles than the grid was planned for: device qsl disagrees
+    // with the host mirror; the tiles past the grid would be left unwritten
+    if (threadIdx.x == 0 && pair_x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+  }
   if (pair_x >= npairs) return;
   const int pair = npairs - 1 - pair_x;  // heaviest (latest) pairs start first
   const int kvh = blockIdx.y;

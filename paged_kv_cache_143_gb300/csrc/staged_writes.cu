@@ -8,7 +8,10 @@
 // One launch, two kinds of CTA that never touch the same cell:
 //  - writer CTAs apply value k of diff w to table[row_w][start_w + k] unless a
 //    later diff also covers that cell (so the result is last-writer-wins in
-//    record order, independent of thread timing);
+//    record order, independent of thread timing). One warp per diff: it first
+//    collects the later diffs of the same row (one coalesced pass over the
+//    later records' rows, O(W) per diff, not per value), then each lane checks
+//    its cells against only those;
 //  - gather CTA i builds gathered[i][c] directly: the value of the latest diff
 //    that covers (idx_mapping[i], c), else the untouched table cell. Covered
 //    cells are never read, uncovered cells are never written: no race.
@@ -19,6 +22,8 @@
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kWriterWarps = kThreads / 32;
+constexpr int kLaterCap = 64;     // later overlapping diffs a writer warp keeps per diff
 constexpr int kRowDiffCap = 512;  // diffs of one row kept in shared memory
 
 struct Diffs {
@@ -52,27 +57,51 @@ __global__ void __launch_bounds__(kThreads) staged_writes_kernel(
 
   if ((int32_t)blockIdx.x < n_writer_ctas) {
     // ------------------------------------------------------------- writers
-    if (d.W == 0) return;
-    const int32_t N = d.offs[d.W];
-    for (int32_t v = blockIdx.x * kThreads + threadIdx.x; v < N; v += n_writer_ctas * kThreads) {
-      // diff w with offs[w] <= v < offs[w+1] (largest w with offs[w] <= v)
-      int32_t lo = 0, hi = d.W - 1;
-      while (lo < hi) {
-        const int32_t mid = (lo + hi + 1) >> 1;
-        if (d.offs[mid] <= v) lo = mid; else hi = mid - 1;
-      }
-      const int32_t w = lo;
-      if (v >= d.offs[w + 1]) continue;  // inside no diff (non-monotone offsets)
+    __shared__ int2 later[kWriterWarps][kLaterCap];  // [start, end) of later same-row diffs
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned full = 0xffffffffu;
+    const int32_t n_warps = n_writer_ctas * kWriterWarps;
+    for (int32_t w = blockIdx.x * kWriterWarps + warp; w < d.W; w += n_warps) {
       if (!diff_valid(d, w, max_reqs, max_blocks)) {
-        if (v == d.offs[w]) pa::raise_error(err, pa::kErrBounds);
+        if (lane == 0) pa::raise_error(err, pa::kErrBounds);
         continue;
       }
-      const int32_t row = d.rows[w];
-      const int32_t col = d.starts[w] + (v - d.offs[w]);
-      bool overwritten = false;
-      for (int32_t w2 = w + 1; w2 < d.W && !overwritten; ++w2)
-        overwritten = diff_covers(d, w2, row, col) && diff_valid(d, w2, max_reqs, max_blocks);
-      if (!overwritten) table[(int64_t)row * max_blocks + col] = d.vals[v];
+      const int32_t row = d.rows[w], start = d.starts[w];
+      const int32_t len = d.offs[w + 1] - d.offs[w];
+      if (len == 0) continue;
+      // the later diffs of this row that overlap [start, start + len)
+      int n_later = 0;
+      bool spilled = false;
+      for (int32_t b = w + 1; b < d.W; b += 32) {
+        const int32_t w2 = b + lane;
+        bool hit = false;
+        int2 iv = make_int2(0, 0);
+        if (w2 < d.W && d.rows[w2] == row && diff_valid(d, w2, max_reqs, max_blocks)) {
+          iv.x = d.starts[w2];
+          iv.y = iv.x + (d.offs[w2 + 1] - d.offs[w2]);
+          hit = iv.x < start + len && iv.y > start;
+        }
+        const unsigned m = __ballot_sync(full, hit);
+        const int k = n_later + __popc(m & ((1u << lane) - 1u));
+        if (hit && k < kLaterCap) later[warp][k] = iv;
+        n_later += __popc(m);
+      }
+      if (n_later > kLaterCap) {
+        spilled = true;
+        n_later = kLaterCap;
+      }
+      __syncwarp();
+      for (int32_t k = lane; k < len; k += 32) {
+        const int32_t col = start + k;
+        bool overwritten = false;
+        for (int i = 0; i < n_later && !overwritten; ++i)
+          overwritten = col >= later[warp][i].x && col < later[warp][i].y;
+        // more overlapping later diffs than the list holds: check the rest
+        for (int32_t w2 = w + 1; spilled && w2 < d.W && !overwritten; ++w2)
+          overwritten = diff_covers(d, w2, row, col) && diff_valid(d, w2, max_reqs, max_blocks);
+        if (!overwritten) table[(int64_t)row * max_blocks + col] = d.vals[d.offs[w] + k];
+      }
+      __syncwarp();
     }
     return;
   }
@@ -126,14 +155,12 @@ extern "C" pa_status pa_apply_staged_writes(int32_t* table, int32_t max_reqs, in
   if (W == 0 && R == 0) return PA_OK;
   unsigned* err = pa::error_word();
   if (!err) return PA_ERR_CUDA;
-  // Writer CTAs: enough to cover W * max_blocks values (the most a valid set
-  // of diffs can carry), capped; they grid-stride over the actual count.
+  // Writer CTAs: one warp per diff, capped; they grid-stride over the diffs.
   int64_t writers = 0;
   if (W > 0) {
-    writers = ((int64_t)W * max_blocks + kThreads - 1) / kThreads;
-    const int64_t cap = (int64_t)pa::num_sms() * 2;
+    writers = ((int64_t)W + kWriterWarps - 1) / kWriterWarps;
+    const int64_t cap = (int64_t)pa::num_sms() * 4;
     if (writers > cap) writers = cap;
-    if (writers < 1) writers = 1;
   }
   const int64_t grid = writers + R;
   if (grid > 0x7FFFFFFF) return PA_ERR_INVALID;

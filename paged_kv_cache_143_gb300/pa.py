@@ -225,11 +225,14 @@ class KVPool:
 
     def ref(self):
         """ctypes reference to the pool's C struct, built once and rebuilt
-        after any attribute is reassigned."""
+        after any attribute is reassigned or either tensor's storage moved
+        (set_, resize_ or .data = ... keep the attribute but change the
+        device pointer)."""
         c = self.__dict__.get("_c")
-        if c is None:
+        k, v = self.__dict__["k"], self.__dict__["v"]
+        if c is None or c[2] != k.data_ptr() or c[3] != v.data_ptr():
             st = self.struct()
-            c = (st, ctypes.byref(st))
+            c = (st, ctypes.byref(st), k.data_ptr(), v.data_ptr())
             self.__dict__["_c"] = c
         return c[1]
 

@@ -184,3 +184,8 @@ def test_pool_struct_is_cached_and_rebuilt_on_reassignment(monkeypatch):
     k2 = torch.zeros_like(k)
     pool.k = k2
     assert read(pool.ref()).k_pool == k2.data_ptr()
+    # the storage moved under the same attribute (set_ swaps it in place)
+    r2 = pool.ref()
+    v2 = torch.zeros_like(v)
+    pool.v.set_(v2)
+    assert pool.ref() is not r2 and read(pool.ref()).v_pool == v2.data_ptr()

@@ -57,8 +57,9 @@ def test_graph_steps_match_oracle_and_eager(cuda_device, kv):
                        v, out, workspace=step.ws)
     before = pa.kernel_launches()
     g.launch()
+    launched = pa.kernel_launches() - before  # pa_get_error launches a kernel of its own
     assert pa.get_error() == pa.PA_OK
-    assert pa.kernel_launches() - before == g.kernels >= 3 * N
+    assert launched == g.kernels >= 3 * N
     assert nc[step.idx.long()].cpu().tolist() == bound
     ref = _oracle_steps(w, ctx, N)
     for s in range(N):

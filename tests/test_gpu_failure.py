@@ -57,3 +57,65 @@ def test_device_seq_lens_disagreeing_with_host_mirror_are_flagged(cuda_device):
     pa.forward(step.q, step.out, step.qsl, step.seq, w.qsl, host_seq, step.gathered,
                step.pool, w.scale, w.causal, workspace=step.ws)
     assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS
+
+
+def _sentinel_out(q, T, extra=8):
+    """An output buffer of T + extra rows filled with a sentinel bit pattern;
+    the library is given its first T rows."""
+    big = torch.empty((T + extra,) + tuple(q.shape[1:]), dtype=torch.bfloat16, device=q.device)
+    big.view(torch.int16).fill_(0x1234)
+    return big, big[:T]
+
+
+def test_device_qsl_past_the_batch_is_flagged_and_never_written(cuda_device):
+    """A device query_start_loc that disagrees with its host mirror and points
+    past the T rows of q / out: the decode, merge and prefill kernels raise
+    PA_ERR_DEVICE_BOUNDS and write nothing beyond row T."""
+    # decodes: request 1 claims token row T + 2 (one token there)
+    w = workloads.build([300, 500, 40], [1, 1, 1], Hq=8, Hkv=2, D=128, B=16, seed=4,
+                        device=cuda_device)
+    step = DeviceStep(w, cuda_device, max_splits=8)
+    step.run()
+    assert pa.get_error() == pa.PA_OK
+    big, out = _sentinel_out(step.q, w.T)
+    bad = torch.tensor([0, w.T + 2, w.T + 3, w.T], dtype=torch.int32, device=cuda_device)
+    pa.forward(step.q, out, bad, step.seq, w.qsl, w.seq_lens, step.gathered, step.pool,
+               w.scale, w.causal, workspace=step.ws)
+    assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS
+    assert (big[w.T:].view(torch.int16) == 0x1234).all()
+
+    # prefill chunks: the last chunk's end moved past T, and the first chunk
+    # made longer than the query tiles the grid was planned for
+    w = workloads.build([300, 200], [100, 50], Hq=8, Hkv=2, D=128, B=16, seed=5,
+                        device=cuda_device)
+    step = DeviceStep(w, cuda_device)
+    step.run()
+    assert pa.get_error() == pa.PA_OK
+    big, out = _sentinel_out(step.q, w.T)
+    for qsl in ([0, 100, w.T + 6], [0, 140, w.T]):
+        bad = torch.tensor(qsl, dtype=torch.int32, device=cuda_device)
+        pa.forward(step.q, out, bad, step.seq, w.qsl, w.seq_lens, step.gathered, step.pool,
+                   w.scale, w.causal, workspace=step.ws)
+        assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS, qsl
+        assert (big[w.T:].view(torch.int16) == 0x1234).all(), qsl
+    # the context is intact
+    step.run()
+    assert pa.get_error() == pa.PA_OK
+
+
+def test_error_raised_on_another_stream_is_never_lost(cuda_device):
+    """pa_get_error reads and clears the error word in one atomic exchange:
+    while a kernel on a second stream is about to raise a bit, repeated reads
+    on the first stream see that bit exactly once, never clearing it unseen."""
+    assert pa.get_error() == pa.PA_OK
+    s2 = torch.cuda.Stream()
+    pa.selftest_wait_timeout(stream=s2)  # raises PA_ERR_TIMEOUT after about 2 s
+    seen = []
+    t0 = time.time()
+    while not s2.query() and time.time() - t0 < 30:
+        seen.append(pa.get_error())
+    s2.synchronize()
+    seen.append(pa.get_error())
+    assert seen.count(pa.PA_ERR_TIMEOUT) == 1, sorted(set(seen))
+    assert all(x in (pa.PA_OK, pa.PA_ERR_TIMEOUT) for x in seen)
+    assert pa.get_error() == pa.PA_OK

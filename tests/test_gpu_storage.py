@@ -141,6 +141,33 @@ def test_staged_writes_many_diffs_on_one_row(cuda_device):
     np.testing.assert_array_equal(g_gat, o_gat)
 
 
+def test_staged_writes_admission_burst(cuda_device):
+    """An admission burst: 1,024 new rows written whole in one call (1,024
+    diffs of up to 512 values), then 1,024 shorter diffs that overwrite parts
+    of random rows; table and gathered rows bit-exact against the oracle."""
+    rng = np.random.default_rng(6)
+    mr, mb = 1024, 512
+    table = rng.integers(-1, 1 << 20, size=(mr, mb)).astype(np.int32)
+    rows = list(range(mr))
+    starts = [0] * mr
+    lens = list(rng.integers(1, mb + 1, size=mr))
+    for _ in range(1024):
+        r, s = int(rng.integers(0, mr)), int(rng.integers(0, mb))
+        rows.append(r)
+        starts.append(s)
+        lens.append(int(rng.integers(0, min(64, mb - s) + 1)))
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    vals = rng.integers(0, 1 << 20, size=int(offs[-1])).astype(np.int32)
+    rows, starts = np.array(rows, np.int32), np.array(starts, np.int32)
+    idx = rng.permutation(mr).astype(np.int32)
+    g_tab, g_gat = _gpu_staged(cuda_device, table, rows, starts, offs, vals, idx)
+    assert pa.get_error() == pa.PA_OK
+    o_tab = table.copy()
+    o_gat = O.apply_staged_writes(o_tab, rows, starts, offs, vals, idx)
+    np.testing.assert_array_equal(g_tab, o_tab)
+    np.testing.assert_array_equal(g_gat, o_gat)
+
+
 def test_staged_writes_out_of_range_are_skipped_and_flagged(cuda_device):
     table = np.arange(12, dtype=np.int32).reshape(3, 4)
     rows = np.array([1, 5, 0], np.int32)       # row 5 is outside the table
