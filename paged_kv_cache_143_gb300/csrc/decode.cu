@@ -496,9 +496,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int k_begin = k_lo + split * p.split_tokens;
   const int k_end = min(seq, k_begin + p.split_tokens);
   const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
-  const int kvh = blockIdx.y;
-  const int g = p.g;
-  const int hq0 = kvh * g;
+  // CTA y serves query heads hq0 .. hq0 + g - 1 of kv head kvh (g <= 16)
+  const int kvh = blockIdx.y / p.head_groups;
+  const int part = blockIdx.y % p.head_groups;
+  const int hq0 = kvh * p.g + 16 * part;
+  const int g = min(16, p.g - 16 * part);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -910,17 +912,22 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cu
   auto k = decode_mma_kernel<D, FP8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(max_splits, p.Hkv, R);
+  dim3 grid(max_splits, p.Hkv * p.head_groups, R);
   k<<<grid, kThreads, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
 // g = 1: one head per kv head, CUDA-core dot products (a 16-row MMA would be
-// 1/16 used); g >= 2: warp-level tensor-core MMAs for all g heads at once.
+// 1/16 used); g >= 2: warp-level tensor-core MMAs for up to 16 heads at once
+// (any g: rows past g are zero padding; g > 16 takes ceil(g / 16) CTAs per
+// kv head, each reading the kv head's keys).
 template <int D, bool FP8>
 cudaError_t launch_decode_d(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
-  if (p.g == 1) return launch_decode_t<D, FP8, 1, 1>(p, R, max_splits, s);
-  if (p.g == 2 || p.g == 4 || p.g == 8 || p.g == 16)
+  if (p.g == 1) {
+    if (p.head_groups != 1) return cudaErrorInvalidValue;
+    return launch_decode_t<D, FP8, 1, 1>(p, R, max_splits, s);
+  }
+  if (p.g >= 2 && p.head_groups == (p.g + 15) / 16)
     return launch_decode_mma_t<D, FP8>(p, R, max_splits, s);
   return cudaErrorInvalidValue;
 }

@@ -53,7 +53,6 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   if (R < 0 || T < 0 || Hq <= 0 || max_blocks < 0) return PA_ERR_INVALID;
   if (Hq % Hkv != 0) return PA_ERR_UNSUPPORTED;
   const int g = Hq / Hkv;
-  if (g != 1 && g != 2 && g != 4 && g != 8 && g != 16) return PA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !std::isfinite(scale)) return PA_ERR_INVALID;
   if (causal != 0 && causal != 1) return PA_ERR_INVALID;
   if (cas && cas->n < 0) return PA_ERR_INVALID;
@@ -77,12 +76,15 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     const int seq = seq_lens_host[r];
     if (seq < ql || (int64_t)seq > (int64_t)max_blocks * B) return PA_ERR_INVALID;
     if (ql > 1) {
+      // a prefill tile (128 rows of token x head) must hold a whole GQA group
+      if (g > 128) return PA_ERR_UNSUPPORTED;
       ++n_pre;
       const int tiles = (ql + 128 / g - 1) / (128 / g);
       if (tiles > max_q_tiles) max_q_tiles = tiles;
     }
   }
   if (R > 65535) return PA_ERR_UNSUPPORTED;
+  if (g > 128 && cas && cas->n > 0) return PA_ERR_UNSUPPORTED;  // prefix tiles, as above
 
   // ---- shared-prefix groups: consecutive decode requests, each with keys
   // past the prefix
@@ -189,6 +191,8 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.g = g;
+    p.head_groups = g > 16 ? (g + 15) / 16 : 1;
+    if ((int64_t)Hkv * p.head_groups > 65535) return PA_ERR_UNSUPPORTED;
     p.k_pool = static_cast<const uint8_t*>(pool->k_pool);
     p.v_pool = static_cast<const uint8_t*>(pool->v_pool);
     p.num_blocks = pool->num_blocks;
@@ -203,7 +207,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     // the workspace holds (a group member's prefix pieces take the first
     // ones). Depends only on seq_lens and the groups, never on placement.
     const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
-    int64_t split = (dec_keys * Hkv + target_ctas - 1) / target_ctas;
+    int64_t split = (dec_keys * Hkv * p.head_groups + target_ctas - 1) / target_ctas;
     split = std::max<int64_t>(split, 256);
     split = std::min<int64_t>(split, max_dec_len);
     split = round_up((int)split, 16);

@@ -46,6 +46,10 @@ struct DecodeParams {
   const int32_t* block_tables; // [R][max_blocks]
   int32_t max_blocks;
   int32_t Hq, Hkv, g;
+  // CTAs per kv head along grid y: 1, or ceil(g / 16) for g > 16 (the MMA
+  // decode serves at most 16 query heads per CTA; CTA y = kv head *
+  // head_groups + part serves heads part * 16 .. of the group)
+  int32_t head_groups;
   const uint8_t* k_pool;       // [num_blocks][Hkv][B][D] elements of 1 or 2 bytes
   const uint8_t* v_pool;
   int32_t num_blocks, B;

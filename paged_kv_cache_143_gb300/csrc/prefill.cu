@@ -11,7 +11,9 @@
 // One CTA = two consecutive tiles (A, B) of 128 query rows x one kv head; both
 // tiles share every K/V tile that is loaded. A tile's rows are the (token,
 // head) pairs of the GQA group that shares the kv head, packed token major
-// (row = token * g + head), so K/V are read once per group.
+// (row = token * g + head), so K/V are read once per group: 128 / g tokens
+// per tile (integer division; when g does not divide 128 the last
+// 128 mod g rows of every tile stay unused, masked to P = 0), g <= 128.
 //   warpgroup 0  warp 0: TMA producer — the Q tiles once (a 4-D tensor map over
 //                [T][Hkv][g][D]), then per 128-key tile one 2-D box per physical
 //                block and 64-column chunk (coordinates from the block table),
@@ -264,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::prefetch_tensormap(&tmap_k);
       tc::prefetch_tensormap(&tmap_v);
       const int nq = ntk[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&bars->q_full, nq * S::kQBytes);
+      // each box holds the tile's (128 / g) * g rows of 64 dims
+      mbar_arrive_expect_tx(&bars->q_full, (uint32_t)(nq * tpt * g * D * 2));
       for (int t = 0; t < nq; ++t)
         for (int c = 0; c < S::kChunks; ++c)
           tc::tma_load_4d(smem + S::kOffQ + t * S::kQRegion + c * S::kChunkBytes, &tmap_q,
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_o = tmem + 2 * kN + t * kN + lane_off;
     const int tok = my_q0 + row / g;
     const int head = row % g;
-    const bool valid_row = my_ntk > 0 && tok < q_len;
+    const bool valid_row = my_ntk > 0 && row < tpt * g && tok < q_len;
     const int limit = !valid_row ? 0 : (p.causal ? min(P + tok + 1, seq) : seq);
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -642,16 +645,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (key0 + k >= limit) s[k] = -INFINITY;
       }
       // raw scores; the log2-domain max is max * scale_log2 (scale > 0);
-      // eight independent partial maxima keep the reduction off one chain
+      // eight independent partial maxima (chain u: columns u + 8 i) keep the
+      // reduction off one dependency chain, three-input maxima halve the
+      // instruction count
       float mx[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = s[u];
+      for (int u = 0; u < 8; ++u) {
+        mx[u] = fmax3(s[u], s[u + 8], s[u + 16]);
 #pragma unroll
-      for (int k = 8; k < kN; k += 8)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], s[k + u]);
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int i = 3; i + 1 < kN / 8; i += 2) mx[u] = fmax3(mx[u], s[u + 8 * i], s[u + 8 * i + 8]);
+        if constexpr ((kN / 8 - 3) % 2 == 1) mx[u] = fmaxf(mx[u], s[u + kN - 8]);
+      }
+      float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       mt *= score_scale;
       float m_use = m_run, alpha = 1.f;
       bool rescale = false;
@@ -664,16 +669,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         rescale = true;
       }
       const float m_sub = m_use == -INFINITY ? 0.f : m_use;
-      float sum[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) sum[u] = 0.f;
+      // p = 2^(s * scale - m) on column pairs: one packed fp32x2 multiply-add
+      // per pair, the exponentials one by one, four packed partial sums
+      const uint64_t sc2 = f2_pack(score_scale, score_scale);
+      const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
+      uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int k = 0; k < kN; k += 8)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          s[k + u] = fast_exp2(fmaf(s[k + u], score_scale, -m_sub));
-          sum[u] += s[k + u];
+        for (int u = 0; u < 4; ++u) {
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(s[k + 2 * u], s[k + 2 * u + 1]), sc2, nm2), a, b);
+          s[k + 2 * u] = fast_exp2(a);
+          s[k + 2 * u + 1] = fast_exp2(b);
+          sum2[u] = f2_add(sum2[u], f2_pack(s[k + 2 * u], s[k + 2 * u + 1]));
         }
+      float sum[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f2_unpack(sum2[u], sum[2 * u], sum[2 * u + 1]);
       l_run = l_run * alpha + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
                                ((sum[4] + sum[5]) + (sum[6] + sum[7])));
       m_run = m_use;
@@ -803,6 +816,7 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   auto encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   const PrefillParams& p = L.p;
+  if (p.g < 1 || p.g > kM) return cudaErrorInvalidValue;  // a tile holds whole GQA groups
   CUtensorMap tq, tk, tv;
   // Q as [T][Hkv][g][D]: box = 64 dims x g heads x 1 kv head x 128/g tokens
   {

@@ -189,3 +189,17 @@ def test_pool_struct_is_cached_and_rebuilt_on_reassignment(monkeypatch):
     v2 = torch.zeros_like(v)
     pool.v.set_(v2)
     assert pool.ref() is not r2 and read(pool.ref()).v_pool == v2.data_ptr()
+
+
+def test_prefill_gqa_wider_than_a_tile_is_refused():
+    """A prefill tile holds 128 rows of token x head: a chunk whose GQA group
+    is wider (g = Hq / Hkv > 128) is refused on the host, before any launch."""
+    import numpy as np
+    L = pa.lib()
+    pool = pa._Pool(16, 16, 4, 16, 1, 64, pa.PA_KV_BF16, 1.0, 1.0)
+    qsl = np.array([0, 3], np.int32)
+    seq = np.array([8], np.int32)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    st = L.pa_forward(16, 16, 16, 16, ptr(qsl), ptr(seq), 16, 4, 1, 3, 256,
+                      ctypes.byref(pool), 0.125, 1, None, 0, None)
+    assert st == pa.PA_ERR_UNSUPPORTED

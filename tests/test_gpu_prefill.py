@@ -49,31 +49,36 @@ def test_prefill_stress_peaky_softmax(cuda_device, q_mult):
     check(w, cuda_device)
 
 
-def _sample_rows(w, n, rng):
-    """Every decode row plus n random prefill rows and the first/last rows of
-    every chunk (token * Hq + head)."""
+def _tile_rows(w, kv_heads=None):
+    """Every decode row, plus whole query tiles of every prefill chunk: the
+    kernel's tile is 128 // g consecutive tokens x the g query heads of one kv
+    head; the tiles at the chunk's start, at the middle of its causal
+    diagonal and at its end, for every kv head (or the kv heads that
+    kv_heads(r, tile) names). Rows are token * Hq + head."""
+    g = w.Hq // w.Hkv
+    tpt = 128 // g
     rows = []
-    ql = np.diff(w.qsl)
     for r in range(w.R):
         a, b = int(w.qsl[r]), int(w.qsl[r + 1])
-        if b - a == 1:
+        ql = b - a
+        if ql == 1:
             rows.extend(a * w.Hq + h for h in range(w.Hq))
-        elif b - a > 1:
-            for t in (a, a + 1, b - 2, b - 1):
-                rows.extend(t * w.Hq + h for h in (0, w.Hq - 1))
-    pre = np.nonzero(np.repeat(ql > 1, ql))[0]
-    toks = rng.choice(pre, size=min(n, pre.size), replace=False)
-    heads = rng.integers(0, w.Hq, size=toks.size)
-    rows.extend((toks * w.Hq + heads).tolist())
+        elif ql > 1:
+            n_tiles = (ql + tpt - 1) // tpt
+            for t in sorted({0, (ql // 2) // tpt, n_tiles - 1}):
+                kvs = range(w.Hkv) if kv_heads is None else kv_heads(r, t)
+                for tok in range(a + t * tpt, min(b, a + (t + 1) * tpt)):
+                    for kv in kvs:
+                        rows.extend(tok * w.Hq + kv * g + j for j in range(g))
     return np.unique(np.array(rows, np.int64))
 
 
 def test_mixed_chunked_prefill_config_full_size(cuda_device):
     """The mixed 4096-token step: 64 decodes + chunks 1024/1024/1920 after
-    prefixes 0/2048/8192; every decode row and a sample of prefill rows."""
+    prefixes 0/2048/8192; every decode row and whole query tiles (start,
+    diagonal middle, end) of every chunk for every kv head."""
     w = workloads.make(3, device=cuda_device)
-    rows = _sample_rows(w, 1500, np.random.default_rng(3))
-    check(w, cuda_device, rows=rows)
+    check(w, cuda_device, rows=_tile_rows(w))
 
 
 def test_mixed_chunked_prefill_reduced_full_compare(cuda_device):
@@ -83,13 +88,20 @@ def test_mixed_chunked_prefill_reduced_full_compare(cuda_device):
     check(w, cuda_device)
 
 
+def _two_kv_heads(w):
+    """Two kv heads per tile, rotating with the chunk and the tile, so every
+    kv head is covered across the chunks (keeps the fp64 oracle's work on the
+    32768-token contexts to a few tens of seconds)."""
+    return lambda r, t: sorted({(r + t) % w.Hkv, (r + t + w.Hkv // 2) % w.Hkv})
+
+
 @pytest.mark.slow
 def test_long_context_bf16_config_full_size(cuda_device):
     """32 requests x 32768 tokens, B 64, 64/8 heads: 8 chunks of 2048 at the
-    end of the context plus 24 decodes; sampled rows."""
+    end of the context plus 24 decodes; every decode row and whole query
+    tiles (start, diagonal middle, end) of every chunk for two kv heads."""
     w = workloads.make(5, device=cuda_device, kv_dtype="bf16")
-    rows = _sample_rows(w, 600, np.random.default_rng(5))
-    check(w, cuda_device, rows=rows)
+    check(w, cuda_device, rows=_tile_rows(w, _two_kv_heads(w)))
 
 
 def test_prefill_invariant_under_block_placement(cuda_device):
@@ -153,5 +165,4 @@ def test_prefill_fp8_query_magnitudes(cuda_device, q_mult):
 @pytest.mark.slow
 def test_long_context_fp8_config_full_size(cuda_device):
     w = workloads.make(5, device=cuda_device, kv_dtype="fp8")
-    rows = _sample_rows(w, 600, np.random.default_rng(6))
-    check(w, cuda_device, rows=rows)
+    check(w, cuda_device, rows=_tile_rows(w, _two_kv_heads(w)))
