@@ -278,10 +278,13 @@ pa_status pa_prepare_inputs(int32_t* num_computed, int32_t max_reqs, const int32
  *              num_q_heads, pool, scale, 1, workspace, workspace_bytes)
  * so every output equals that of the eager calls made with the same bound.
  * The forward plan is fixed at creation from seq_len_bound_host; every launch
- * must keep each request's sequence length (num_computed + 1 at each step) at
- * or below its bound, else the kernels set PA_ERR_DEVICE_BOUNDS (no read out
- * of range). The table must already hold the blocks of every position the
- * steps write; block_tables holds the rows table[idx_mapping[i]].
+ * should keep each request's sequence length (num_computed + 1 at each step)
+ * at or below its bound. A length past its bound is either still covered by
+ * the plan, with exact results (the persistent GQA decode of pa_forward cuts
+ * the device-side lengths into its CTA ranges at every launch, within the
+ * workspace's split slots), or refused with PA_ERR_DEVICE_BOUNDS; nothing is
+ * ever read out of range. The table must already hold the blocks of every
+ * position the steps write; block_tables holds the rows table[idx_mapping[i]].
  *
  * The pool struct, pointers and sizes are read at creation and baked into the
  * graph: the buffers must stay allocated and in place until destroy. The

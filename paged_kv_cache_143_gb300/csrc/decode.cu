@@ -94,8 +94,8 @@ struct SmemTail {
   int abort;
 };
 
-// The producer warp of both decode kernels: the warp fetches the block ids of
-// 32 chunks at a time (lane i: chunk base + i, one coalesced load). Per 16-key
+// The producer warp of the decode kernels: it fetches the block ids of 32
+// chunks at a time (lane i: chunk base + i, one coalesced load). Per 16-key
 // chunk, K and V are each one contiguous run of the pool, moved by one bulk
 // async copy each that completes on the stage's mbarrier by transaction
 // bytes. The producer handles a group of chunks per step (lane i waits for
@@ -104,19 +104,22 @@ struct SmemTail {
 // chunks in flight. kTma: the same runs move as TMA tensor boxes (16 rows of
 // 128 codes, 128-byte swizzle) through the maps tk and tv, which view a pool
 // as [block][kv head * B + offset][128].
+// produce_run issues chunks [0, nch) of one key run (keys k_begin + 16 c of
+// the block-table row `table`, kv head kvh) into ring positions q_base + c
+// (stage = position mod kStages); it returns false if a wait gave up or the
+// CTA aborted, and adds the positions it issued to *issued (the drain must
+// wait for every one of them).
 template <class G, bool kTma>
-__device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
-                                        int r, int kvh, int k_begin, int nch, int lane,
-                                        const CUtensorMap* tk, const CUtensorMap* tv) {
+__device__ __forceinline__ bool produce_run(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
+                                            const int32_t* table, int kvh, int k_begin, int nch,
+                                            int64_t q_base, int lane, const CUtensorMap* tk,
+                                            const CUtensorMap* tv, int64_t* issued) {
   // chunks handled per step (half the ring, at most 8)
   constexpr int kGroup = G::kStages / 2 < 8 ? G::kStages / 2 : 8;
   static_assert(32 % kGroup == 0, "groups must tile the 32 chunks of a block-id fetch");
   const unsigned full = 0xffffffffu;
-  const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
   const int64_t head_stride = (int64_t)p.B * G::kRowBytes;  // one (block, head)
-  int issued = 0;
-  bool ok = true;
-  for (int base = 0; base < nch && ok; base += 32) {
+  for (int base = 0; base < nch; base += 32) {
     const int c_lane = base + lane;
     const int key_lane = k_begin + c_lane * kChunk;
     int blk_lane = c_lane < nch ? __ldg(table + key_lane / p.B) : 0;
@@ -131,15 +134,17 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
     const int n = min(32, nch - base);
     for (int g0 = 0; g0 < n; g0 += kGroup) {
       const int gn = min(kGroup, n - g0);
-      const int c = base + g0 + lane;  // this lane's chunk of the group
+      const int64_t q = q_base + base + g0 + lane;  // this lane's ring position
       const bool mine = lane < gn;
-      const int stage = c % G::kStages, round = c / G::kStages;
+      const int stage = (int)(q % G::kStages);
+      const int64_t round = q / G::kStages;
       bool free_ok = true;
       if (mine && round > 0) free_ok = mbar_wait(&tail->empty[stage], (round - 1) & 1, p.err);
-      ok = __all_sync(full, free_ok) && !*reinterpret_cast<volatile int*>(&tail->abort);
+      const bool ok = __all_sync(full, free_ok) && !*reinterpret_cast<volatile int*>(&tail->abort);
       if (!ok) {
         if (lane == 0) tail->abort = 1;
-        break;
+        *issued = q_base + base + g0;
+        return false;
       }
       if constexpr (kTma) {
         const int y = __shfl_sync(full, y_lane, (g0 + lane) & 31);
@@ -159,14 +164,31 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
           bulk_g2s(dst + G::kChunkBytes, p.v_pool + off, G::kChunkBytes, &tail->full[stage]);
         }
       }
-      issued = base + g0 + gn;
     }
   }
-  // drain: every issued copy has landed before the CTA may exit
-  if (lane == 0) {
-    for (int c = issued - G::kStages > 0 ? issued - G::kStages : 0; c < issued; ++c)
-      mbar_wait(&tail->full[c % G::kStages], (c / G::kStages) & 1, p.err);
-  }
+  *issued = q_base + nch;
+  return true;
+}
+
+// Waits until the copies of ring positions [0, issued) have landed (those
+// still in flight are the last kStages), so that the CTA may exit.
+template <class G>
+__device__ __forceinline__ void drain(const DecodeParams& p, SmemTail* tail, int64_t issued,
+                                      int lane) {
+  if (lane == 0)
+    for (int64_t q = issued - G::kStages > 0 ? issued - G::kStages : 0; q < issued; ++q)
+      mbar_wait(&tail->full[q % G::kStages], (q / G::kStages) & 1, p.err);
+}
+
+// The whole producer of a one-run CTA: request r's key run, then the drain.
+template <class G, bool kTma>
+__device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, SmemTail* tail,
+                                        int r, int kvh, int k_begin, int nch, int lane,
+                                        const CUtensorMap* tk, const CUtensorMap* tv) {
+  const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
+  int64_t issued = 0;
+  produce_run<G, kTma>(p, ring, tail, table, kvh, k_begin, nch, 0, lane, tk, tv, &issued);
+  drain<G>(p, tail, issued, lane);
 }
 
 // GH heads per warp, HG head groups per CTA (GH * HG = g).
@@ -425,10 +447,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 //
 // Per kv head the decode contraction is [g x D] . [D x keys] with g <= 16,
 // below the smallest tcgen05 tile (M = 64), so each consumer warp issues
-// mma.sync m16n8k16 (f32 accumulate) on register fragments: the g query
-// heads are the 16 rows (padded with zero rows), a 16-key chunk is two n8
-// tiles. The operands come straight from the linear rows the bulk copies
-// deliver:
+// mma.sync m16n8k16 (f32 accumulate) on register fragments: up to 16 query
+// rows (padded with zero rows), a 16-key chunk is two n8 tiles. The operands
+// come straight from the linear rows the bulk copies deliver:
 //  - S = Q K^T: a fixed permutation of the head dimension, the same for Q and
 //    K, maps k-steps 2j and 2j+1 of lane (grp, tig) onto the 8 contiguous
 //    dims 32 j + 8 tig .. +7, so every K fragment is one 16-byte load of
@@ -447,95 +468,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
 // 2 tig + 1 of its K row (the head-dimension permutation becomes: k-step
 // pair j of lane tig = dims 32 tig + 8 j .. +7) and chunk grp of its V rows,
 // and every 16-byte load of a quarter-warp falls on distinct banks.
+//
+// MmaRows holds one warp's state for up to 16 query rows: the Q fragments,
+// the per-row score scale, and the running (O, max, sum) of the rows.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 2)
-    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
+struct MmaRows {
+  static constexpr int KJ = D / 32;  // pairs of k-steps
+  static constexpr int DG = D / 8;   // output dims per lane group = n-tiles of O
+  static constexpr bool kSw = FP8 && D == 128;  // swizzled stages (TMA tensor copies)
   using G = Geo<D, FP8>;
-  constexpr int kStages = G::kStages;
-  constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
-  constexpr int KJ = D / 32;       // pairs of k-steps
-  constexpr int DG = D / 8;        // output dims per lane group = n-tiles of O
-  constexpr bool kSw = FP8 && D == 128;  // swizzled stages (TMA tensor copies)
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  if constexpr (kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;  // 1024-byte aligned
-  float* comb_o = reinterpret_cast<float*>(ring + kStages * G::kStageBytes);  // [4][16][D]
-  float* comb_m = comb_o + kConsumerWarps * kRows * D;                       // [4][16]
-  float* comb_l = comb_m + kConsumerWarps * kRows;                           // [4][16]
-  SmemTail* tail = reinterpret_cast<SmemTail*>(comb_l + kConsumerWarps * kRows);
+  uint32_t qa[KJ][2][4];  // qa[j][row][w] = the 16-bit pair of dims 32j + 8tig + 2w
+  float sc[2];            // score scale of rows grp and grp + 8 (log2 units)
+  float o[DG][4];
+  float m[2], l[2];
 
-  const int r = blockIdx.z;
-  const int qs = p.qsl[r];
-  if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
-  if (qs < 0 || qs >= p.T) {  // a device qsl that leaves q / out
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-    return;
-  }
-  const int seq = p.seq_lens[r];
-  if (seq < 1 || seq > p.max_blocks * p.B) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-    return;
-  }
-  // keys [k_lo, seq): all of them, or the private tail after a shared prefix
-  const int grp_id = group_of(p.groups, r);
-  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
-  const int slot0 = prefix_slots(p.groups, grp_id);  // a member's prefix pieces come first
-  if (k_lo >= seq) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-    return;
-  }
-  const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
-  if (nsplit > (int)gridDim.x || (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
-    // device seq_lens disagree with the host mirror
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-    return;
-  }
-  const int split = blockIdx.x;
-  if (split >= nsplit) return;
-  const int k_begin = k_lo + split * p.split_tokens;
-  const int k_end = min(seq, k_begin + p.split_tokens);
-  const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
-  // CTA y serves query heads hq0 .. hq0 + g - 1 of kv head kvh (g <= 16)
-  const int kvh = blockIdx.y / p.head_groups;
-  const int part = blockIdx.y % p.head_groups;
-  const int hq0 = kvh * p.g + 16 * part;
-  const int g = min(16, p.g - 16 * part);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&tail->full[i], 1);
-      mbar_init(&tail->empty[i], 1);
-    }
-    tail->abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp == kConsumerWarps) {
-    if (kSw && lane == 0) {
-      tc::prefetch_tensormap(&tmap_k);
-      tc::prefetch_tensormap(&tmap_v);
-    }
-    produce<G, kSw>(p, ring, tail, r, kvh, k_begin, nch, lane, &tmap_k, &tmap_v);
-    return;
-  }
-
-  const int grp = lane >> 2, tig = lane & 3;
-  const unsigned full = 0xffffffffu;
-  // ---- Q fragments: qa[j][row][w] = the 16-bit pair of dims 32j + 8tig + 2w
-  uint32_t qa[KJ][2][4];
-  float sc[2];  // score scale of rows grp and grp + 8 (log2 units)
-  {
+  // Loads rows grp and grp + 8 (rows[ri], nullptr: a zero padding row; a
+  // row may sit in global or in shared memory).
+  __device__ __forceinline__ void load_q(const __nv_bfloat16* const (&rows)[2], float q_scale,
+                                         int tig) {
+    const unsigned full = 0xffffffffu;
     float qf[2][KJ][8];
 #pragma unroll
     for (int ri = 0; ri < 2; ++ri) {
-      const int row = grp + 8 * ri;
 #pragma unroll
       for (int j = 0; j < KJ; ++j) {
-        if (row < g) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-              p.q + ((int64_t)qs * p.Hq + hq0 + row) * D + (kSw ? 32 * tig + 8 * j : 32 * j + 8 * tig)));
+        if (rows[ri]) {  // a global or a shared-memory row
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              rows[ri] + (kSw ? 32 * tig + 8 * j : 32 * j + 8 * tig));
           bf16x8_to_f32(v, qf[ri][j]);
         } else {
 #pragma unroll
@@ -546,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int ri = 0; ri < 2; ++ri) {
       float up = 1.f;
-      sc[ri] = p.q_scale;
+      sc[ri] = q_scale;
       if (FP8) {
         float amax = 0.f;
 #pragma unroll
@@ -577,8 +536,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
   }
-  auto mma = [](float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                uint32_t b1) {
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int nt = 0; nt < DG; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  static __device__ __forceinline__ void mma(float (&c)[4], uint32_t a0, uint32_t a1,
+                                             uint32_t a2, uint32_t a3, uint32_t b0,
+                                             uint32_t b1) {
     if (FP8)
       asm volatile(
           "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
@@ -591,17 +559,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           "{%8,%9}, {%0,%1,%2,%3};"
           : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
           : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-  };
+  }
   // 8 E4M3 codes -> four f16 pairs (exact)
-  auto widen8 = [](uint32_t x, uint32_t y, uint32_t* w) {
+  static __device__ __forceinline__ void widen8(uint32_t x, uint32_t y, uint32_t* w) {
     asm("{\n\t.reg .b16 a, b, c, d;\n\tmov.b32 {a, b}, %4;\n\tmov.b32 {c, d}, %5;\n\t"
         "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t"
         "cvt.rn.f16x2.e4m3x2 %2, c;\n\tcvt.rn.f16x2.e4m3x2 %3, d;\n\t}"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
         : "r"(x), "r"(y));
-  };
+  }
   // 8 consecutive elements of a row -> four 16-bit pairs
-  auto load8 = [&](const uint8_t* src, uint32_t (&w)[4]) {
+  static __device__ __forceinline__ void load8(const uint8_t* src, uint32_t (&w)[4]) {
     if (FP8) {
       const uint2 v = *reinterpret_cast<const uint2*>(src);
       widen8(v.x, v.y, w);
@@ -609,25 +577,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint4 v = *reinterpret_cast<const uint4*>(src);
       w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
     }
-  };
+  }
 
-  float o[DG][4];
-#pragma unroll
-  for (int nt = 0; nt < DG; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-  bool ok = true;
-  for (int c = warp; c < nch && ok; c += kConsumerWarps) {
-    const int stage = c % kStages, round = c / kStages;
-    if (!__all_sync(full, mbar_wait(&tail->full[stage], round & 1, p.err))) {
-      tail->abort = 1;
-      ok = false;
-      break;
-    }
-    const uint8_t* Ks = ring + stage * G::kStageBytes;
-    const uint8_t* Vs = Ks + G::kChunkBytes;
-    const int key0 = k_begin + c * kChunk;
-
+  // One 16-key chunk (K rows Ks, V rows Vs, keys key0 .. key0 + 15, those at
+  // or past k_end masked): scores, online softmax, O += P V.
+  __device__ __forceinline__ void chunk(const uint8_t* Ks, const uint8_t* Vs, int key0, int k_end,
+                                        int grp, int tig) {
+    const unsigned full = 0xffffffffu;
     // S for keys 8t + grp (B fragments), t = n-tile
     float s[2][4];
 #pragma unroll
@@ -679,14 +635,14 @@ __global__ void __launch_bounds__(kThreads, 2)
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
       const float m_new = fmaxf(m[ri], mx);
-      alpha[ri] = exp2f(m[ri] - m_new);
+      alpha[ri] = ex2_ftz(m[ri] - m_new);
       float ps = 0.f;
 #pragma unroll
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float& x = s[t][2 * ri + e];
-          x = exp2f(x - m_new);
+          x = ex2_ftz(x - m_new);
           ps += x;
         }
       l[ri] = l[ri] * alpha[ri] + ps;
@@ -749,54 +705,535 @@ __global__ void __launch_bounds__(kThreads, 2)
       asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b1) : "r"(vw[2][nt >> 1]), "r"(vw[3][nt >> 1]), "r"(sel));
       mma(o[nt], pa[0], pa[1], pa[2], pa[3], b0, b1);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&tail->empty[stage]);
   }
 
-  // per-row sums over the four lanes of a row
+  // Per-row sums over the four lanes of a row (the maxima already agree).
+  __device__ __forceinline__ void finish_sums() {
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    l[ri] += __shfl_xor_sync(full, l[ri], 1);
-    l[ri] += __shfl_xor_sync(full, l[ri], 2);
+    for (int ri = 0; ri < 2; ++ri) {
+      l[ri] += __shfl_xor_sync(0xffffffffu, l[ri], 1);
+      l[ri] += __shfl_xor_sync(0xffffffffu, l[ri], 2);
+    }
   }
+
+  // This warp's rows into the combine buffer of warp `warp` (rows < nrows).
+  __device__ __forceinline__ void to_comb(float* comb_o, float* comb_m, float* comb_l, int warp,
+                                          int nrows, int grp, int tig) const {
 #pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    const int row = grp + 8 * ri;
-    if (row < g) {
+    for (int ri = 0; ri < 2; ++ri) {
+      const int row = grp + 8 * ri;
+      if (row < nrows) {
 #pragma unroll
-      for (int nt = 0; nt < DG; ++nt)
+        for (int nt = 0; nt < DG; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
-          comb_o[(warp * kRows + row) * D + DG * (2 * tig + e) + nt] = o[nt][2 * ri + e];
-      if (tig == 0) {
-        comb_m[warp * kRows + row] = m[ri];
-        comb_l[warp * kRows + row] = l[ri];
+          for (int e = 0; e < 2; ++e)
+            comb_o[(warp * 16 + row) * D + DG * (2 * tig + e) + nt] = o[nt][2 * ri + e];
+        if (tig == 0) {
+          comb_m[warp * 16 + row] = m[ri];
+          comb_l[warp * 16 + row] = l[ri];
+        }
       }
     }
   }
-  named_bar_sync(1, kConsumerWarps * 32);
-  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
+};
 
-  for (int idx = threadIdx.x; idx < g * D; idx += kConsumerWarps * 32) {
+// Combines the four consumer warps' partial rows (comb buffers) of one key
+// run and writes rows hq0 .. hq0 + nrows - 1 of request r: the bf16 output
+// (direct), or the fp32 partial into split slot `slot`.
+template <int D>
+__device__ __forceinline__ void combine_rows(const DecodeParams& p, const float* comb_o,
+                                             const float* comb_m, const float* comb_l, int nrows,
+                                             int r, int qs, int hq0, bool direct, int slot) {
+  for (int idx = threadIdx.x; idx < nrows * D; idx += kConsumerWarps * 32) {
     const int row = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * kRows + row]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * 16 + row]);
     float L = 0.f, O = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = exp2f(comb_m[w * kRows + row] - M);  // 0 for a warp with no chunk
-      L += f * comb_l[w * kRows + row];
-      O += f * comb_o[(w * kRows + row) * D + d];
+      const float f = exp2f(comb_m[w * 16 + row] - M);  // 0 for a warp with no chunk
+      L += f * comb_l[w * 16 + row];
+      O += f * comb_o[(w * 16 + row) * D + d];
     }
     const int hq = hq0 + row;
-    if (slot0 + nsplit == 1) {
+    if (direct) {
       p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
     } else {
-      const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + slot0 + split;
+      const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + slot;
       p.ws_o[orow * D + d] = O * p.v_scale;
       if (d == 0) p.ws_ml[orow] = make_float2(M, L);
     }
+  }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
+  using G = Geo<D, FP8>;
+  using MR = MmaRows<D, FP8>;
+  constexpr int kStages = G::kStages;
+  constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  if constexpr (MR::kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;  // 1024-byte aligned
+  float* comb_o = reinterpret_cast<float*>(ring + kStages * G::kStageBytes);  // [4][16][D]
+  float* comb_m = comb_o + kConsumerWarps * kRows * D;                       // [4][16]
+  float* comb_l = comb_m + kConsumerWarps * kRows;                           // [4][16]
+  SmemTail* tail = reinterpret_cast<SmemTail*>(comb_l + kConsumerWarps * kRows);
+
+  const int r = blockIdx.z;
+  const int qs = p.qsl[r];
+  if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
+  if (qs < 0 || qs >= p.T) {  // a device qsl that leaves q / out
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int seq = p.seq_lens[r];
+  if (seq < 1 || seq > p.max_blocks * p.B) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  // keys [k_lo, seq): all of them, or the private tail after a shared prefix
+  const int grp_id = group_of(p.groups, r);
+  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
+  const int slot0 = prefix_slots(p.groups, grp_id);  // a member's prefix pieces come first
+  if (k_lo >= seq) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  if (nsplit > (int)gridDim.x || (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
+    // device seq_lens disagree with the host mirror
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int split = blockIdx.x;
+  if (split >= nsplit) return;
+  const int k_begin = k_lo + split * p.split_tokens;
+  const int k_end = min(seq, k_begin + p.split_tokens);
+  const int nch = (k_end - k_begin + kChunk - 1) / kChunk;
+  // CTA y serves query heads hq0 .. hq0 + g - 1 of kv head kvh (g <= 16)
+  const int kvh = blockIdx.y / p.head_groups;
+  const int part = blockIdx.y % p.head_groups;
+  const int hq0 = kvh * p.g + 16 * part;
+  const int g = min(16, p.g - 16 * part);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->empty[i], 1);
+    }
+    tail->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kConsumerWarps) {
+    if (MR::kSw && lane == 0) {
+      tc::prefetch_tensormap(&tmap_k);
+      tc::prefetch_tensormap(&tmap_v);
+    }
+    produce<G, MR::kSw>(p, ring, tail, r, kvh, k_begin, nch, lane, &tmap_k, &tmap_v);
+    return;
+  }
+
+  const int grp = lane >> 2, tig = lane & 3;
+  const unsigned full = 0xffffffffu;
+  MR st;
+  {
+    const __nv_bfloat16* rows[2];
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri) {
+      const int row = grp + 8 * ri;
+      rows[ri] = row < g ? p.q + ((int64_t)qs * p.Hq + hq0 + row) * D : nullptr;
+    }
+    st.load_q(rows, p.q_scale, tig);
+  }
+  st.reset();
+  for (int c = warp; c < nch; c += kConsumerWarps) {
+    const int stage = c % kStages, round = c / kStages;
+    if (!__all_sync(full, mbar_wait(&tail->full[stage], round & 1, p.err))) {
+      tail->abort = 1;
+      break;
+    }
+    const uint8_t* Ks = ring + stage * G::kStageBytes;
+    st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->empty[stage]);
+  }
+  st.finish_sums();
+  st.to_comb(comb_o, comb_m, comb_l, warp, g, grp, tig);
+  named_bar_sync(1, kConsumerWarps * 32);
+  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
+  combine_rows<D>(p, comb_o, comb_m, comb_l, g, r, qs, hq0, slot0 + nsplit == 1, slot0 + split);
+}
+
+// ---------------------------------------------------------------------------
+// Persistent GQA decode (2 <= g <= 16), see PersistPlan: CTA b streams the
+// chunks [b Q, b Q + Q) of the call's flat chunk space, unit after unit,
+// without draining its ring between them: the producer warp runs ahead
+// across unit boundaries, so the start of each unit (its Q fragments, its
+// first copies) overlaps the end of the previous one, and every CTA gets the
+// same number of chunks whatever the lengths. Tail units: the chunks go
+// round-robin to the four consumer warps (by ring position), which combine
+// through shared memory at the unit's end. Shared-prefix units: every warp
+// reads every chunk for its own 16 rows (16 / g members x g heads), and
+// writes its rows' partials itself; the ring position's empty barrier counts
+// four arrivals either way.
+struct Seg {
+  int kind;        // 0: shared-prefix unit, 1: decode tail
+  int r;           // tail: the request; prefix: the member block's first request
+  int n_members;   // prefix: requests of the member block
+  int grp;         // group (-1: none)
+  int kvh;
+  int c0, c1;      // chunks [c0, c1) of the unit
+  int key0;        // key of the unit's chunk 0
+  int key_end;     // keys at or past it are masked
+  int piece, n_pieces;
+  int64_t f_next;  // flat position after this piece
+};
+
+__device__ __forceinline__ Seg segment_at(const DecodeParams& p, const int32_t* pref,
+                                          const int32_t* rseq, int64_t f, int64_t f_end,
+                                          int64_t Q) {
+  Seg sg;
+  const int64_t Wp = p.pp.pre_base[p.groups.n];
+  int64_t a, C, w;
+  if (f < Wp) {
+    int k = 0;
+    while (k + 1 < p.groups.n && p.pp.pre_base[k + 1] <= f) ++k;
+    const int Mb = p.pp.members_per_block;
+    const int nblk = (p.groups.size[k] + Mb - 1) / Mb;
+    C = p.groups.prefix_tokens[k] / kChunk;
+    w = kPrefixWeight;
+    const int64_t u = (f - p.pp.pre_base[k]) / (C * w);
+    const int mb = (int)(u % nblk);
+    sg.kind = 0;
+    sg.grp = k;
+    sg.kvh = (int)(u / nblk);
+    sg.r = p.groups.first[k] + mb * Mb;
+    sg.n_members = min(Mb, p.groups.size[k] - mb * Mb);
+    sg.key0 = 0;
+    sg.key_end = p.groups.prefix_tokens[k];
+    a = p.pp.pre_base[k] + u * C * w;
+  } else {
+    // the request r with Hkv pref[r] <= t < Hkv pref[r + 1] (units of no chunk
+    // are skipped: their pref does not grow)
+    const int64_t t = f - Wp;
+    int lo = 0, hi = p.R - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((int64_t)p.Hkv * pref[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    C = pref[lo + 1] - pref[lo];
+    w = 1;
+    const int64_t off = t - (int64_t)p.Hkv * pref[lo];
+    sg.kind = 1;
+    sg.r = lo;
+    sg.n_members = 1;
+    sg.grp = group_of(p.groups, lo);
+    sg.kvh = (int)(off / C);
+    sg.key0 = sg.grp >= 0 ? p.groups.prefix_tokens[sg.grp] : 0;
+    sg.key_end = rseq[lo];
+    a = Wp + (int64_t)p.Hkv * pref[lo] + (int64_t)sg.kvh * C;
+  }
+  // the unit's chunks whose start lies in [f, f_end): chunk i starts at a + w i
+  sg.c0 = (int)((f - a + w - 1) / w);
+  sg.c1 = (int)min(C, (f_end - a + w - 1) / w);
+  sg.piece = (int)((a + w * sg.c0) / Q - a / Q);
+  sg.n_pieces = (int)flat_pieces(a, C, w, Q);
+  sg.f_next = min(a + w * C, f_end);  // > f: f lies inside the unit
+  return sg;
+}
+
+// Chunks of request r's decode tail (0 if r is not a decode request; a bad
+// device entry raises kErrBounds and counts 0).
+__device__ __forceinline__ int tail_chunks(const DecodeParams& p, int r) {
+  const int qs = p.qsl[r];
+  if (p.qsl[r + 1] - qs != 1) return 0;
+  const int seq = p.seq_lens[r];
+  const int grp = group_of(p.groups, r);
+  const int k_lo = grp >= 0 ? p.groups.prefix_tokens[grp] : 0;
+  if (qs < 0 || qs >= p.T || seq < 1 || seq > p.max_blocks * p.B || k_lo >= seq) {
+    raise_error(p.err, kErrBounds);
+    return 0;
+  }
+  return (seq - k_lo + kChunk - 1) / kChunk;
+}
+
+// Staged query rows of the persistent decode: up to kQSlots tail units ahead.
+constexpr int kQSlots = 8;
+constexpr int kQStageBytes = 8192;
+struct PersistBars {
+  uint64_t q_full[kQSlots];   // a unit's query rows landed (transaction bytes)
+  uint64_t q_empty[kQSlots];  // the four consumer warps have read them
+  SmemTail t;
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_persist_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
+  using G = Geo<D, FP8>;
+  using MR = MmaRows<D, FP8>;
+  constexpr int kStages = G::kStages;
+  constexpr int kRows = 16;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  if constexpr (MR::kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;
+  float* comb_o = reinterpret_cast<float*>(ring + kStages * G::kStageBytes);  // [4][16][D]
+  float* comb_m = comb_o + kConsumerWarps * kRows * D;                       // [4][16]
+  float* comb_l = comb_m + kConsumerWarps * kRows;                           // [4][16]
+  int32_t* pref = reinterpret_cast<int32_t*>(comb_l + kConsumerWarps * kRows);  // [R + 1]
+  int32_t* rtok = pref + kMaxPersistR + 4;  // [R] each request's token (decodes)
+  int32_t* rseq = rtok + kMaxPersistR;      // [R] and its sequence length
+  // the query rows of the next tail units, staged by the producer: kQSlots
+  // slots of g rows each (as many as fit kQStageBytes)
+  __nv_bfloat16* qstage = reinterpret_cast<__nv_bfloat16*>(rseq + kMaxPersistR);
+  PersistBars* pb = reinterpret_cast<PersistBars*>(reinterpret_cast<uint8_t*>(qstage) +
+                                                   kQStageBytes);
+  SmemTail* tail = &pb->t;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = p.R;
+  const int q_slot_elems = p.g * D;  // one tail unit's g query rows
+  const int n_qslots = min(kQSlots, kQStageBytes / (q_slot_elems * 2));
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->empty[i], kConsumerWarps);
+    }
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(&pb->q_full[i], 1);
+      mbar_init(&pb->q_empty[i], kConsumerWarps);
+    }
+    tail->abort = 0;
+    fence_mbar_init();
+  }
+  // the tails' chunk counts (then their exclusive running sum, warp 0), and
+  // each request's token and length, kept for the units below
+  for (int r = tid; r < R; r += kThreads) {
+    pref[r] = tail_chunks(p, r);
+    rtok[r] = pref[r] > 0 ? p.qsl[r] : -1;
+    rseq[r] = pref[r] > 0 ? p.seq_lens[r] : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < R; base += 32) {
+      const int v = base + lane < R ? pref[base + lane] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (base + lane < R) pref[base + lane] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) pref[R] = carry;
+  }
+  __syncthreads();
+  const int64_t W = (int64_t)p.pp.pre_base[p.groups.n] + (int64_t)p.Hkv * pref[R];
+  const int64_t Q =
+      max((W + (int64_t)gridDim.x - 1) / (int64_t)gridDim.x, (int64_t)max(p.pp.q_min, 1));
+  if (blockIdx.x == 0) {  // the plan, for the merge kernel
+    if (tid == 0) {
+      p.pp.aux[0] = (int32_t)Q;
+      p.pp.aux[1] = (int32_t)W;
+      if (W > (int64_t)gridDim.x * Q) raise_error(p.err, kErrBounds);  // chunks no CTA takes
+    }
+    for (int r = tid; r <= R; r += kThreads) p.pp.aux[2 + r] = pref[r];
+  }
+  const int64_t f_begin = (int64_t)blockIdx.x * Q;
+  const int64_t f_end = min(W, f_begin + Q);
+  if (f_begin >= f_end) return;
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------- producer
+    if (MR::kSw && lane == 0) {
+      tc::prefetch_tensormap(&tmap_k);
+      tc::prefetch_tensormap(&tmap_v);
+    }
+    int64_t q = 0, issued = 0;
+    int n_tail = 0;  // tail units whose query rows were staged
+    bool ok = true;
+    for (int64_t f = f_begin; f < f_end;) {
+      const Seg sg = segment_at(p, pref, rseq, f, f_end, Q);
+      if (sg.f_next <= f) break;  // cannot happen: f lies inside the unit
+      f = sg.f_next;
+      const int nch = sg.c1 - sg.c0;
+      if (nch <= 0) continue;  // the range holds no chunk start of this unit
+      if (sg.kind == 1) {
+        // the unit's g query rows (contiguous in q) into the next staging slot,
+        // once the consumers have read the unit that used it before
+        const int slot = n_tail % n_qslots, use = n_tail / n_qslots;
+        if (lane == 0) {
+          if (use > 0) ok = mbar_wait(&pb->q_empty[slot], (use - 1) & 1, p.err);
+          if (ok) {
+            mbar_arrive_expect_tx(&pb->q_full[slot], (unsigned)(q_slot_elems * 2));
+            bulk_g2s(qstage + slot * q_slot_elems,
+                     p.q + ((int64_t)rtok[sg.r] * p.Hq + (int64_t)sg.kvh * p.g) * D,
+                     (unsigned)(q_slot_elems * 2), &pb->q_full[slot]);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          if (lane == 0) tail->abort = 1;
+          break;
+        }
+        ++n_tail;
+      }
+      const int row = sg.kind ? sg.r : p.groups.first[sg.grp];
+      const int32_t* table = p.block_tables + (int64_t)row * p.max_blocks;
+      if (!produce_run<G, MR::kSw>(p, ring, tail, table, sg.kvh, sg.key0 + sg.c0 * kChunk, nch,
+                                   q, lane, &tmap_k, &tmap_v, &issued))
+        break;
+      q += nch;
+    }
+    drain<G>(p, tail, issued, lane);
+    // and the staged query rows still in flight (the last use of each slot)
+    if (lane == 0)
+      for (int u = n_tail - n_qslots > 0 ? n_tail - n_qslots : 0; u < n_tail; ++u)
+        mbar_wait(&pb->q_full[u % n_qslots], (u / n_qslots) & 1, p.err);
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int grp = lane >> 2, tig = lane & 3;
+  const unsigned full = 0xffffffffu;
+  const int g = p.g;
+  const int mpw = 16 / g;  // members per warp in a shared-prefix unit
+  int64_t q = 0;           // ring position of the unit's first chunk
+  int n_tail = 0;          // tail units started (their query rows are staged)
+  bool ok = true;
+  MR st;
+  for (int64_t f = f_begin; f < f_end;) {
+    const Seg sg = segment_at(p, pref, rseq, f, f_end, Q);
+    if (sg.f_next <= f) break;  // (as the producer)
+    f = sg.f_next;
+    const int nch = sg.c1 - sg.c0;
+    if (nch <= 0) continue;  // (as the producer)
+    const int k_begin = sg.key0 + sg.c0 * kChunk;
+    const int k_end = min(sg.key_end, sg.key0 + sg.c1 * kChunk);
+    if (sg.kind == 1) {
+      // ----- a decode tail: rows = the g heads of the request's token,
+      // staged in shared memory by the producer
+      const int qs = rtok[sg.r];
+      const int hq0 = sg.kvh * g;
+      {
+        const int slot = n_tail % n_qslots;
+        if (!__all_sync(full, mbar_wait(&pb->q_full[slot], (n_tail / n_qslots) & 1, p.err))) {
+          tail->abort = 1;
+          ok = false;
+        }
+        const __nv_bfloat16* rows[2];
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+          const int row = grp + 8 * ri;
+          rows[ri] = ok && row < g ? qstage + slot * q_slot_elems + row * D : nullptr;
+        }
+        st.load_q(rows, p.q_scale, tig);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pb->q_empty[slot]);  // the rows are in registers
+        ++n_tail;
+      }
+      st.reset();
+      // chunk c sits at ring position q + c and belongs to warp (q + c) mod 4
+      for (int c = (int)((warp - q % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+           ok && c < nch; c += kConsumerWarps) {
+        const int64_t pos = q + c;
+        const int stage = (int)(pos % kStages);
+        if (!__all_sync(full, mbar_wait(&tail->full[stage], (pos / kStages) & 1, p.err))) {
+          tail->abort = 1;
+          ok = false;
+          break;
+        }
+        const uint8_t* Ks = ring + stage * G::kStageBytes;
+        st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cnt(&tail->empty[stage], kConsumerWarps);
+      }
+      st.finish_sums();
+      st.to_comb(comb_o, comb_m, comb_l, warp, g, grp, tig);
+      named_bar_sync(1, kConsumerWarps * 32);
+      const bool direct = sg.grp < 0 && sg.n_pieces == 1;
+      const int slot = prefix_pieces_of(p, sg.grp, sg.kvh, sg.r, Q) + sg.piece;
+      if (!direct && slot >= p.ws_splits) {
+        if (tid == 0) raise_error(p.err, kErrBounds);  // device lengths disagree with the plan
+      } else if (ok) {
+        combine_rows<D>(p, comb_o, comb_m, comb_l, g, sg.r, qs, hq0, direct, slot);
+      }
+    } else {
+      // ----- a shared-prefix unit: this warp's members x the g heads
+      const int m0 = sg.r + warp * mpw;
+      const int nm = max(0, min(mpw, sg.r + sg.n_members - m0));
+      const int nrows = nm * g;
+      int tok[2] = {0, 0};
+      {
+        const __nv_bfloat16* rows[2];
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+          const int row = grp + 8 * ri;
+          rows[ri] = nullptr;
+          if (row < nrows) {
+            tok[ri] = p.qsl[m0 + row / g];
+            if (tok[ri] >= 0 && tok[ri] < p.T)  // (tail_chunks flags a bad entry)
+              rows[ri] = p.q + ((int64_t)tok[ri] * p.Hq + sg.kvh * g + row % g) * D;
+          }
+        }
+        st.load_q(rows, p.q_scale, tig);
+      }
+      st.reset();
+      for (int c = 0; ok && c < nch; ++c) {
+        const int64_t pos = q + c;
+        const int stage = (int)(pos % kStages);
+        if (!__all_sync(full, mbar_wait(&tail->full[stage], (pos / kStages) & 1, p.err))) {
+          tail->abort = 1;
+          ok = false;
+          break;
+        }
+        if (nrows > 0) {
+          const uint8_t* Ks = ring + stage * G::kStageBytes;
+          st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->empty[stage]);
+      }
+      st.finish_sums();
+      if (ok && sg.piece >= p.ws_splits) {
+        if (lane == 0) raise_error(p.err, kErrBounds);
+      } else if (ok) {
+        // the partial of each row: o * v_scale unnormalised, (max, sum) in
+        // log2 units, in split slot `piece` of the member's query head
+#pragma unroll
+        for (int ri = 0; ri < 2; ++ri) {
+          const int row = grp + 8 * ri;
+          if (row < nrows) {
+            const int member = m0 + row / g;
+            const int64_t wrow =
+                ((int64_t)member * p.Hq + sg.kvh * g + row % g) * p.ws_splits + sg.piece;
+            float* wo = p.ws_o + wrow * D;
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+              for (int nt = 0; nt < MR::DG; nt += 4)
+                *reinterpret_cast<float4*>(wo + MR::DG * (2 * tig + e) + nt) =
+                    make_float4(st.o[nt][2 * ri + e] * p.v_scale,
+                                st.o[nt + 1][2 * ri + e] * p.v_scale,
+                                st.o[nt + 2][2 * ri + e] * p.v_scale,
+                                st.o[nt + 3][2 * ri + e] * p.v_scale);
+            if (tig == 0) p.ws_ml[wrow] = make_float2(st.m[ri], st.l[ri]);
+          }
+        }
+      }
+    }
+    q += nch;
+    // every consumer warp takes the same decision (and the comb buffer is
+    // free again for the next unit)
+    if (named_bar_or(2, kConsumerWarps * 32, !ok || *reinterpret_cast<volatile int*>(&tail->abort)))
+      break;
   }
 }
 
@@ -818,8 +1255,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeParams p)
   const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
   if (k_lo >= seq) return;
   // slots: the shared-prefix pieces (group members) and the splits
-  const int nsplit =
-      prefix_slots(p.groups, grp_id) + (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  int nsplit;
+  if (p.pp.on) {
+    // the persistent kernel's partition, as it recorded it
+    const int64_t Q = p.pp.aux[0];
+    const int32_t* pref = p.pp.aux + 2;
+    const int64_t C = pref[r + 1] - pref[r];
+    if (C <= 0 || Q <= 0) return;
+    const int kvh = h / p.g;
+    const int64_t a = p.pp.pre_base[p.groups.n] + (int64_t)p.Hkv * pref[r] + kvh * C;
+    const int nt = (int)flat_pieces(a, C, 1, Q);
+    if (grp_id < 0 && nt == 1) return;  // the decode kernel wrote the output
+    nsplit = prefix_pieces_of(p, grp_id, kvh, r, Q) + nt;
+  } else {
+    nsplit = prefix_slots(p.groups, grp_id) + (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  }
   if (nsplit <= 1 || nsplit > p.ws_splits) return;
   const int64_t row0 = ((int64_t)r * p.Hq + h) * p.ws_splits;
   const unsigned full = 0xffffffffu;
@@ -883,37 +1333,67 @@ cudaError_t launch_decode_t(const DecodeParams& p, int R, int max_splits, cudaSt
   return cudaGetLastError();
 }
 
+// TMA maps of the E4M3 pools at D = 128 (the swizzled stages): a pool as
+// [block][kv head * B + offset][128 codes]; one box = one 16-key chunk of one
+// kv head, 128-byte swizzled. Left empty for the other kernels.
 template <int D, bool FP8>
-cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
-  constexpr bool kSw = FP8 && D == 128;
-  constexpr int smem = (kSw ? 1024 : 0) + Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
-                       kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
-  CUtensorMap tk{}, tv{};  // unused by the unswizzled kernels
-  if constexpr (kSw) {
+cudaError_t decode_maps(const DecodeParams& p, CUtensorMap* tk, CUtensorMap* tv) {
+  *tk = CUtensorMap{};
+  *tv = CUtensorMap{};
+  if constexpr (FP8 && D == 128) {
     auto encode = tensor_map_encoder();
     if (!encode) return cudaErrorNotSupported;
     if (p.num_blocks < 1) return cudaErrorInvalidValue;
-    // a pool as [block][kv head * B + offset][128 codes]; one box = one 16-key
-    // chunk of one kv head, 128-byte swizzled
     cuuint64_t dims[3] = {128, (cuuint64_t)p.Hkv * p.B, (cuuint64_t)p.num_blocks};
     cuuint64_t strides[2] = {128, (cuuint64_t)p.Hkv * p.B * 128};
     cuuint32_t box[3] = {128, (cuuint32_t)kChunk, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    if (encode(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.k_pool), dims,
+    if (encode(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.k_pool), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-        encode(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.v_pool), dims,
+        encode(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.v_pool), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  return cudaSuccess;
+}
+
+template <int D, bool FP8>
+cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cudaStream_t s) {
+  constexpr bool kSw = FP8 && D == 128;
+  constexpr int smem = (kSw ? 1024 : 0) + Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
+                       kConsumerWarps * 16 * (D + 2) * 4 + (int)sizeof(SmemTail);
+  CUtensorMap tk, tv;
+  cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
+  if (e != cudaSuccess) return e;
   auto k = decode_mma_kernel<D, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(max_splits, p.Hkv * p.head_groups, R);
   k<<<grid, kThreads, smem, s>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool FP8>
+cudaError_t launch_decode_persist_t(const DecodeParams& p, int n_cta, cudaStream_t s) {
+  constexpr bool kSw = FP8 && D == 128;
+  constexpr int smem = (kSw ? 1024 : 0) + Geo<D, FP8>::kStages * Geo<D, FP8>::kStageBytes +
+                       kConsumerWarps * 16 * (D + 2) * 4 + (3 * kMaxPersistR + 4) * 4 +
+                       kQStageBytes + (int)sizeof(PersistBars);
+  static_assert(2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM");
+  if (p.g < 2 || p.g > 16 || p.head_groups != 1 || p.R > kMaxPersistR || p.R < 1 || !p.pp.on ||
+      !p.pp.aux)
+    return cudaErrorInvalidValue;
+  CUtensorMap tk, tv;
+  cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
+  if (e != cudaSuccess) return e;
+  auto k = decode_persist_kernel<D, FP8>;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  k<<<n_cta, kThreads, smem, s>>>(tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -941,6 +1421,15 @@ cudaError_t launch_decode(const DecodeParams& p, int D, bool fp8, int R, int max
                : launch_decode_d<128, false>(p, R, max_splits, s);
   return fp8 ? launch_decode_d<64, true>(p, R, max_splits, s)
              : launch_decode_d<64, false>(p, R, max_splits, s);
+}
+
+cudaError_t launch_decode_persist(const DecodeParams& p, int D, bool fp8, int n_cta,
+                                  cudaStream_t s) {
+  if (D == 128)
+    return fp8 ? launch_decode_persist_t<128, true>(p, n_cta, s)
+               : launch_decode_persist_t<128, false>(p, n_cta, s);
+  return fp8 ? launch_decode_persist_t<64, true>(p, n_cta, s)
+             : launch_decode_persist_t<64, false>(p, n_cta, s);
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int D, int R, cudaStream_t s) {

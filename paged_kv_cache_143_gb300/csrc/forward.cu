@@ -21,12 +21,20 @@ size_t split_row_bytes(int64_t R, int64_t Hq, int64_t D) {
 
 int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+// The workspace starts with the persistent decode's plan area (see
+// pa::PersistPlan), then the split partials: fp32 o [R][Hq][S][D], then
+// (max, sum) [R][Hq][S].
+size_t plan_area_bytes(int64_t R) {
+  return (size_t)((pa::persist_aux_words(R) * 4 + 255) / 256 * 256);
+}
+
 }  // namespace
 
 extern "C" size_t pa_forward_workspace_size(int32_t num_reqs, int32_t num_q_heads,
                                             int32_t head_dim, int32_t max_splits) {
   if (num_reqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_splits <= 0) return 0;
-  return split_row_bytes(num_reqs, num_q_heads, head_dim) * (size_t)max_splits;
+  return plan_area_bytes(num_reqs) +
+         split_row_bytes(num_reqs, num_q_heads, head_dim) * (size_t)max_splits;
 }
 
 namespace {
@@ -110,7 +118,9 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     }
   }
   const size_t row_bytes = split_row_bytes(R, Hq, D);
-  const int64_t ws_splits = row_bytes ? (int64_t)(workspace_bytes / row_bytes) : 0;
+  const size_t plan_bytes = plan_area_bytes(R);
+  const size_t part_bytes = workspace_bytes > plan_bytes ? workspace_bytes - plan_bytes : 0;
+  const int64_t ws_splits = row_bytes ? (int64_t)(part_bytes / row_bytes) : 0;
   // the pieces of a prefix and at least one tail split each need a slot
   if (gd.n > 0 && ws_splits < 2) return PA_ERR_INVALID;
   int pieces = 0, pairs_per_piece = 0;
@@ -148,8 +158,8 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   cudaStream_t s = pa::as_stream(stream);
   const bool fp8 = pool->dtype == PA_KV_FP8_E4M3;
   const float kLog2e = 1.4426950408889634f;
-  float* ws_o = static_cast<float*>(workspace);
-  float2* ws_ml = reinterpret_cast<float2*>(static_cast<uint8_t*>(workspace) +
+  float* ws_o = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + plan_bytes);
+  float2* ws_ml = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(ws_o) +
                                             (size_t)R * Hq * ws_splits * D * 4);
 
   auto prefill_launch = [&]() {
@@ -179,6 +189,63 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     return L;
   };
 
+  // ---- persistent GQA decode: the decode work as one flat chunk space cut
+  // into equal per-CTA ranges (pa::PersistPlan)
+  pa::PersistPlan pp{};
+  int persist_ctas = 0;
+  if (n_dec > 0 && g >= 2 && g <= 16 && R <= pa::kMaxPersistR && ws_splits >= 2 &&
+      gd.n == 0) {
+    const int M = 4 * (16 / g);
+    pp.members_per_block = M;
+    int64_t wp = 0;
+    for (int k = 0; k < gd.n; ++k) {
+      pp.pre_base[k] = (int32_t)wp;
+      const int64_t nblk = (gd.size[k] + M - 1) / M;
+      wp += (int64_t)Hkv * nblk * (gd.prefix_tokens[k] / 16) * pa::kPrefixWeight;
+    }
+    pp.pre_base[gd.n] = (int32_t)wp;
+    int64_t W = wp;
+    for (int r = 0; r < R; ++r) {
+      if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+      int k_lo;
+      group_slots(r, &k_lo);
+      W += (int64_t)Hkv * ((seq_lens_host[r] - k_lo + 15) / 16);
+    }
+    // slots a request may need with Q units per CTA: the chunk starts of a
+    // unit of C chunks of cost w span w (C - 1) units, so they fall into at
+    // most ceil(w (C - 1) / Q) + 1 CTA ranges (1 if Q >= W)
+    auto unit_slots = [&](int64_t C, int64_t w, int64_t Q) -> int64_t {
+      return Q >= W ? 1 : (w * (C - 1) + Q - 1) / Q + 1;
+    };
+    auto fits = [&](int64_t Q) {
+      for (int r = 0; r < R; ++r) {
+        if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+        int k_lo;
+        group_slots(r, &k_lo);
+        const int k = pa::group_of(gd, r);
+        int64_t need = unit_slots((seq_lens_host[r] - k_lo + 15) / 16, 1, Q);
+        if (k >= 0) need += unit_slots(gd.prefix_tokens[k] / 16, pa::kPrefixWeight, Q);
+        if (need > ws_splits) return false;
+      }
+      return true;
+    };
+    // every CTA range must hold a chunk start: Q >= kPrefixWeight
+    int64_t lo = pa::kPrefixWeight, hi = std::max<int64_t>(W, lo);  // fits(W) holds
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) / 2;
+      if (fits(mid)) hi = mid; else lo = mid + 1;
+    }
+    const int64_t q_min = lo;
+    const int64_t n_max = (int64_t)pa::num_sms() * 2;  // two CTAs per SM
+    const int64_t Q = std::max(q_min, (W + n_max - 1) / n_max);
+    if (W > 0 && W < INT32_MAX && Q < INT32_MAX) {
+      pp.on = 1;
+      pp.q_min = (int32_t)q_min;
+      pp.aux = static_cast<int32_t*>(workspace);
+      persist_ctas = (int)((W + Q - 1) / Q);
+    }
+  }
+
   if (n_dec > 0) {
     pa::DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
@@ -201,6 +268,8 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     p.v_scale = fp8 ? pool->v_scale : 1.f;
     p.err = err;
     p.groups = gd;
+    p.R = R;
+    p.pp = pp;
 
     // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
     // least 256 keys, a multiple of the 16-key chunk; bounded by the slots
@@ -248,6 +317,17 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
       p.ws_o = ws_o;
       p.ws_ml = ws_ml;
     }
+    if (pp.on) {
+      // every decode (tails and the groups' prefixes) in one persistent launch,
+      // then the merge of the pieces
+      p.ws_splits = (int)ws_splits;
+      p.ws_o = ws_o;
+      p.ws_ml = ws_ml;
+      if (pa::launch_decode_persist(p, D, fp8, persist_ctas, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+    } else {
     if (gd.n > 0) {  // the prefix pieces of every group, into slots 0..pieces-1
       pa::PrefillLaunch L = prefill_launch();
       L.p.mode = 1;
@@ -267,6 +347,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     if (need > 1) {
       if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
       pa::count_launches(1);
+    }
     }
   }
 

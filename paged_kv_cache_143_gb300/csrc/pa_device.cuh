@@ -52,6 +52,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
       : "memory");
 }
 
+// One arrival that counts as `count` of the barrier's expected arrivals.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, unsigned count) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(count)
+      : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"
@@ -108,6 +117,22 @@ __device__ __forceinline__ void named_bar_sync(unsigned id, unsigned count) {
   asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier over `count` threads that also ORs a predicate over them:
+// every participant gets the same answer (for decisions that must agree).
+__device__ __forceinline__ bool named_bar_or(unsigned id, unsigned count, bool pred) {
+  __syncwarp();
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------------------ numbers
 
 // Two fp32 lanes in one 64-bit register pair, for the sm_100-family packed
@@ -136,6 +161,14 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// 2^x on the special-function unit, results below 2^-126 flushed to zero
+// (softmax weights: exp2(-inf) = 0, exp2(0) = 1 exactly).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // max(a, b, c) in one instruction (sm_100 family)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;

@@ -59,7 +59,11 @@ def test_status_strings_and_host_side_rejections():
 
 
 def test_workspace_size_formula():
-    assert pa.forward_workspace_size(256, 32, 128, 4) == 256 * 32 * 4 * (128 * 4 + 8)
+    # the plan area of the persistent decode (R + 3 int32 words, rounded up to
+    # 256 bytes), then per split slot an fp32 partial row and its (max, sum)
+    plan = (4 * (256 + 3) + 255) // 256 * 256
+    assert pa.forward_workspace_size(256, 32, 128, 4) == plan + 256 * 32 * 4 * (128 * 4 + 8)
+    assert pa.forward_workspace_size(1, 1, 64, 1) == 256 + (64 * 4 + 8)
     assert pa.forward_workspace_size(0, 32, 128, 4) == 0
 
 

@@ -43,7 +43,10 @@ def test_noalloc_forward_matches_workspace_forward_twice(cuda_device):
 def test_noalloc_rejects_scratch_beyond_its_maximum(cuda_device):
     w = workloads.build([100, 40], [1, 1], Hq=8, Hkv=8, D=128, B=16, seed=3, device=cuda_device)
     step = DeviceStep(w, cuda_device, max_splits=0)
-    too_many = pa.NOALLOC_SCRATCH_BYTES // pa.forward_workspace_size(w.R, w.Hq, w.D, 1) + 1
+    # the scratch grows by one split row per split: one more split than the
+    # array holds rows for is always beyond it
+    row = pa.forward_workspace_size(w.R, w.Hq, w.D, 2) - pa.forward_workspace_size(w.R, w.Hq, w.D, 1)
+    too_many = pa.NOALLOC_SCRATCH_BYTES // row + 1
     with pytest.raises(pa.PaError) as e:
         pa.forward_noalloc(step.q, step.out, step.qsl, step.seq, w.qsl, w.seq_lens,
                            step.table[:w.R], step.pool, w.scale, 1, max_splits=int(too_many))
