@@ -740,22 +740,39 @@ struct MmaRows {
 // Combines the four consumer warps' partial rows (comb buffers) of one key
 // run and writes rows hq0 .. hq0 + nrows - 1 of request r: the bf16 output
 // (direct), or the fp32 partial into split slot `slot`.
+// All 128 consumer threads must call it (it holds a barrier).
 template <int D>
 __device__ __forceinline__ void combine_rows(const DecodeParams& p, const float* comb_o,
-                                             const float* comb_m, const float* comb_l, int nrows,
-                                             int r, int qs, int hq0, bool direct, int slot) {
-  for (int idx = threadIdx.x; idx < nrows * D; idx += kConsumerWarps * 32) {
-    const int row = idx / D, d = idx % D;
+                                             float* comb_m, float* comb_l, int nrows, int r,
+                                             int qs, int hq0, bool direct, int slot) {
+  // each row's warp weights 2^(m_w - M) (0 for a warp with no chunk), its
+  // max and its sum, once per row: thread t < nrows owns row t and replaces
+  // the row's comb_m entries by the weights, its warp-0 and warp-1 comb_l
+  // entries by the sum and the max
+  if ((int)threadIdx.x < nrows) {
+    const int row = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, comb_m[w * 16 + row]);
-    float L = 0.f, O = 0.f;
+    float L = 0.f, f[kConsumerWarps];
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) {
-      const float f = exp2f(comb_m[w * 16 + row] - M);  // 0 for a warp with no chunk
-      L += f * comb_l[w * 16 + row];
-      O += f * comb_o[(w * 16 + row) * D + d];
+      f[w] = ex2_ftz(comb_m[w * 16 + row] - M);
+      L += f[w] * comb_l[w * 16 + row];
     }
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) comb_m[w * 16 + row] = f[w];
+    comb_l[row] = L;
+    comb_l[16 + row] = M;
+  }
+  named_bar_sync(3, kConsumerWarps * 32);
+  for (int idx = threadIdx.x; idx < nrows * D; idx += kConsumerWarps * 32) {
+    const int row = idx / D, d = idx % D;
+    const float L = comb_l[row], M = comb_l[16 + row];
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w)
+      O += comb_m[w * 16 + row] * comb_o[(w * 16 + row) * D + d];
     const int hq = hq0 + row;
     if (direct) {
       p.out[((int64_t)qs * p.Hq + hq) * D + d] = __float2bfloat16_rn(O / L * p.v_scale);
@@ -865,8 +882,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   st.finish_sums();
   st.to_comb(comb_o, comb_m, comb_l, warp, g, grp, tig);
-  named_bar_sync(1, kConsumerWarps * 32);
-  if (*reinterpret_cast<volatile int*>(&tail->abort)) return;
+  // one decision for all consumer threads (combine_rows holds a barrier)
+  if (named_bar_or(1, kConsumerWarps * 32, *reinterpret_cast<volatile int*>(&tail->abort)))
+    return;
   combine_rows<D>(p, comb_o, comb_m, comb_l, g, r, qs, hq0, slot0 + nsplit == 1, slot0 + split);
 }
 
@@ -874,23 +892,16 @@ __global__ void __launch_bounds__(kThreads, 2)
 // Persistent GQA decode (2 <= g <= 16), see PersistPlan: CTA b streams the
 // chunks [b Q, b Q + Q) of the call's flat chunk space, unit after unit,
 // without draining its ring between them: the producer warp runs ahead
-// across unit boundaries, so the start of each unit (its Q fragments, its
-// first copies) overlaps the end of the previous one, and every CTA gets the
-// same number of chunks whatever the lengths. Tail units: the chunks go
-// round-robin to the four consumer warps (by ring position), which combine
-// through shared memory at the unit's end. Shared-prefix units: every warp
-// reads every chunk for its own 16 rows (16 / g members x g heads), and
-// writes its rows' partials itself; the ring position's empty barrier counts
-// four arrivals either way.
+// across unit boundaries (and stages each unit's query rows with one bulk
+// copy), so the start of each unit overlaps the end of the previous one, and
+// every CTA gets the same number of chunks whatever the request lengths.
+// Within a unit the chunks go round-robin to the four consumer warps (by ring
+// position), which combine through shared memory at the unit's end.
 struct Seg {
-  int kind;        // 0: shared-prefix unit, 1: decode tail
-  int r;           // tail: the request; prefix: the member block's first request
-  int n_members;   // prefix: requests of the member block
-  int grp;         // group (-1: none)
+  int r;           // the request
   int kvh;
   int c0, c1;      // chunks [c0, c1) of the unit
-  int key0;        // key of the unit's chunk 0
-  int key_end;     // keys at or past it are masked
+  int key_end;     // keys at or past it are masked (the sequence length)
   int piece, n_pieces;
   int64_t f_next;  // flat position after this piece
 };
@@ -898,69 +909,40 @@ struct Seg {
 __device__ __forceinline__ Seg segment_at(const DecodeParams& p, const int32_t* pref,
                                           const int32_t* rseq, int64_t f, int64_t f_end,
                                           int64_t Q) {
-  Seg sg;
-  const int64_t Wp = p.pp.pre_base[p.groups.n];
-  int64_t a, C, w;
-  if (f < Wp) {
-    int k = 0;
-    while (k + 1 < p.groups.n && p.pp.pre_base[k + 1] <= f) ++k;
-    const int Mb = p.pp.members_per_block;
-    const int nblk = (p.groups.size[k] + Mb - 1) / Mb;
-    C = p.groups.prefix_tokens[k] / kChunk;
-    w = kPrefixWeight;
-    const int64_t u = (f - p.pp.pre_base[k]) / (C * w);
-    const int mb = (int)(u % nblk);
-    sg.kind = 0;
-    sg.grp = k;
-    sg.kvh = (int)(u / nblk);
-    sg.r = p.groups.first[k] + mb * Mb;
-    sg.n_members = min(Mb, p.groups.size[k] - mb * Mb);
-    sg.key0 = 0;
-    sg.key_end = p.groups.prefix_tokens[k];
-    a = p.pp.pre_base[k] + u * C * w;
-  } else {
-    // the request r with Hkv pref[r] <= t < Hkv pref[r + 1] (units of no chunk
-    // are skipped: their pref does not grow)
-    const int64_t t = f - Wp;
-    int lo = 0, hi = p.R - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if ((int64_t)p.Hkv * pref[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    C = pref[lo + 1] - pref[lo];
-    w = 1;
-    const int64_t off = t - (int64_t)p.Hkv * pref[lo];
-    sg.kind = 1;
-    sg.r = lo;
-    sg.n_members = 1;
-    sg.grp = group_of(p.groups, lo);
-    sg.kvh = (int)(off / C);
-    sg.key0 = sg.grp >= 0 ? p.groups.prefix_tokens[sg.grp] : 0;
-    sg.key_end = rseq[lo];
-    a = Wp + (int64_t)p.Hkv * pref[lo] + (int64_t)sg.kvh * C;
+  // the request r with Hkv pref[r] <= f < Hkv pref[r + 1] (requests of no
+  // chunk are skipped: their pref does not grow)
+  int lo = 0, hi = p.R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)p.Hkv * pref[mid] <= f) lo = mid; else hi = mid - 1;
   }
-  // the unit's chunks whose start lies in [f, f_end): chunk i starts at a + w i
-  sg.c0 = (int)((f - a + w - 1) / w);
-  sg.c1 = (int)min(C, (f_end - a + w - 1) / w);
-  sg.piece = (int)((a + w * sg.c0) / Q - a / Q);
-  sg.n_pieces = (int)flat_pieces(a, C, w, Q);
-  sg.f_next = min(a + w * C, f_end);  // > f: f lies inside the unit
+  const int64_t C = pref[lo + 1] - pref[lo];
+  const int64_t off = f - (int64_t)p.Hkv * pref[lo];
+  Seg sg;
+  sg.r = lo;
+  sg.kvh = (int)(off / C);
+  sg.key_end = rseq[lo];
+  const int64_t a = (int64_t)p.Hkv * pref[lo] + (int64_t)sg.kvh * C;
+  const int64_t end = min(a + C, f_end);  // > f: f lies inside the unit
+  sg.c0 = (int)(f - a);
+  sg.c1 = (int)(end - a);
+  sg.piece = (int)(f / Q - a / Q);
+  sg.n_pieces = (int)flat_pieces(a, C, Q);
+  sg.f_next = end;
   return sg;
 }
 
-// Chunks of request r's decode tail (0 if r is not a decode request; a bad
-// device entry raises kErrBounds and counts 0).
+// Chunks of request r's keys (0 if r is not a decode request; a bad device
+// entry raises kErrBounds and counts 0).
 __device__ __forceinline__ int tail_chunks(const DecodeParams& p, int r) {
   const int qs = p.qsl[r];
   if (p.qsl[r + 1] - qs != 1) return 0;
   const int seq = p.seq_lens[r];
-  const int grp = group_of(p.groups, r);
-  const int k_lo = grp >= 0 ? p.groups.prefix_tokens[grp] : 0;
-  if (qs < 0 || qs >= p.T || seq < 1 || seq > p.max_blocks * p.B || k_lo >= seq) {
+  if (qs < 0 || qs >= p.T || seq < 1 || seq > p.max_blocks * p.B) {
     raise_error(p.err, kErrBounds);
     return 0;
   }
-  return (seq - k_lo + kChunk - 1) / kChunk;
+  return (seq + kChunk - 1) / kChunk;
 }
 
 // Staged query rows of the persistent decode: up to kQSlots tail units ahead.
@@ -1036,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (lane == 0) pref[R] = carry;
   }
   __syncthreads();
-  const int64_t W = (int64_t)p.pp.pre_base[p.groups.n] + (int64_t)p.Hkv * pref[R];
+  const int64_t W = (int64_t)p.Hkv * pref[R];
   const int64_t Q =
       max((W + (int64_t)gridDim.x - 1) / (int64_t)gridDim.x, (int64_t)max(p.pp.q_min, 1));
   if (blockIdx.x == 0) {  // the plan, for the merge kernel
@@ -1065,8 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (sg.f_next <= f) break;  // cannot happen: f lies inside the unit
       f = sg.f_next;
       const int nch = sg.c1 - sg.c0;
-      if (nch <= 0) continue;  // the range holds no chunk start of this unit
-      if (sg.kind == 1) {
+      {
         // the unit's g query rows (contiguous in q) into the next staging slot,
         // once the consumers have read the unit that used it before
         const int slot = n_tail % n_qslots, use = n_tail / n_qslots;
@@ -1085,10 +1066,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         ++n_tail;
       }
-      const int row = sg.kind ? sg.r : p.groups.first[sg.grp];
-      const int32_t* table = p.block_tables + (int64_t)row * p.max_blocks;
-      if (!produce_run<G, MR::kSw>(p, ring, tail, table, sg.kvh, sg.key0 + sg.c0 * kChunk, nch,
-                                   q, lane, &tmap_k, &tmap_v, &issued))
+      const int32_t* table = p.block_tables + (int64_t)sg.r * p.max_blocks;
+      if (!produce_run<G, MR::kSw>(p, ring, tail, table, sg.kvh, sg.c0 * kChunk, nch, q, lane,
+                                   &tmap_k, &tmap_v, &issued))
         break;
       q += nch;
     }
@@ -1104,9 +1084,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int grp = lane >> 2, tig = lane & 3;
   const unsigned full = 0xffffffffu;
   const int g = p.g;
-  const int mpw = 16 / g;  // members per warp in a shared-prefix unit
-  int64_t q = 0;           // ring position of the unit's first chunk
-  int n_tail = 0;          // tail units started (their query rows are staged)
+  int64_t q = 0;   // ring position of the unit's first chunk
+  int n_tail = 0;  // units started (their query rows are staged)
   bool ok = true;
   MR st;
   for (int64_t f = f_begin; f < f_end;) {
@@ -1114,125 +1093,61 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (sg.f_next <= f) break;  // (as the producer)
     f = sg.f_next;
     const int nch = sg.c1 - sg.c0;
-    if (nch <= 0) continue;  // (as the producer)
-    const int k_begin = sg.key0 + sg.c0 * kChunk;
-    const int k_end = min(sg.key_end, sg.key0 + sg.c1 * kChunk);
-    if (sg.kind == 1) {
-      // ----- a decode tail: rows = the g heads of the request's token,
-      // staged in shared memory by the producer
-      const int qs = rtok[sg.r];
-      const int hq0 = sg.kvh * g;
-      {
-        const int slot = n_tail % n_qslots;
-        if (!__all_sync(full, mbar_wait(&pb->q_full[slot], (n_tail / n_qslots) & 1, p.err))) {
-          tail->abort = 1;
-          ok = false;
-        }
-        const __nv_bfloat16* rows[2];
+    const int k_begin = sg.c0 * kChunk;
+    const int k_end = min(sg.key_end, sg.c1 * kChunk);
+    // rows: the g heads of the request's token, staged by the producer
+    const int qs = rtok[sg.r];
+    const int hq0 = sg.kvh * g;
+    {
+      const int slot = n_tail % n_qslots;
+      if (!__all_sync(full, mbar_wait(&pb->q_full[slot], (n_tail / n_qslots) & 1, p.err))) {
+        tail->abort = 1;
+        ok = false;
+      }
+      const __nv_bfloat16* rows[2];
 #pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-          const int row = grp + 8 * ri;
-          rows[ri] = ok && row < g ? qstage + slot * q_slot_elems + row * D : nullptr;
-        }
-        st.load_q(rows, p.q_scale, tig);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pb->q_empty[slot]);  // the rows are in registers
-        ++n_tail;
+      for (int ri = 0; ri < 2; ++ri) {
+        const int row = grp + 8 * ri;
+        rows[ri] = ok && row < g ? qstage + slot * q_slot_elems + row * D : nullptr;
       }
-      st.reset();
-      // chunk c sits at ring position q + c and belongs to warp (q + c) mod 4
-      for (int c = (int)((warp - q % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
-           ok && c < nch; c += kConsumerWarps) {
-        const int64_t pos = q + c;
-        const int stage = (int)(pos % kStages);
-        if (!__all_sync(full, mbar_wait(&tail->full[stage], (pos / kStages) & 1, p.err))) {
-          tail->abort = 1;
-          ok = false;
-          break;
-        }
-        const uint8_t* Ks = ring + stage * G::kStageBytes;
-        st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cnt(&tail->empty[stage], kConsumerWarps);
+      st.load_q(rows, p.q_scale, tig);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pb->q_empty[slot]);  // the rows are in registers
+      ++n_tail;
+    }
+    st.reset();
+    // chunk c sits at ring position q + c and belongs to warp (q + c) mod 4
+    for (int c = (int)((warp - q % kConsumerWarps + kConsumerWarps) % kConsumerWarps);
+         ok && c < nch; c += kConsumerWarps) {
+      const int64_t pos = q + c;
+      const int stage = (int)(pos % kStages);
+      if (!__all_sync(full, mbar_wait(&tail->full[stage], (pos / kStages) & 1, p.err))) {
+        tail->abort = 1;
+        ok = false;
+        break;
       }
-      st.finish_sums();
-      st.to_comb(comb_o, comb_m, comb_l, warp, g, grp, tig);
-      named_bar_sync(1, kConsumerWarps * 32);
-      const bool direct = sg.grp < 0 && sg.n_pieces == 1;
-      const int slot = prefix_pieces_of(p, sg.grp, sg.kvh, sg.r, Q) + sg.piece;
-      if (!direct && slot >= p.ws_splits) {
-        if (tid == 0) raise_error(p.err, kErrBounds);  // device lengths disagree with the plan
-      } else if (ok) {
-        combine_rows<D>(p, comb_o, comb_m, comb_l, g, sg.r, qs, hq0, direct, slot);
-      }
-    } else {
-      // ----- a shared-prefix unit: this warp's members x the g heads
-      const int m0 = sg.r + warp * mpw;
-      const int nm = max(0, min(mpw, sg.r + sg.n_members - m0));
-      const int nrows = nm * g;
-      int tok[2] = {0, 0};
-      {
-        const __nv_bfloat16* rows[2];
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-          const int row = grp + 8 * ri;
-          rows[ri] = nullptr;
-          if (row < nrows) {
-            tok[ri] = p.qsl[m0 + row / g];
-            if (tok[ri] >= 0 && tok[ri] < p.T)  // (tail_chunks flags a bad entry)
-              rows[ri] = p.q + ((int64_t)tok[ri] * p.Hq + sg.kvh * g + row % g) * D;
-          }
-        }
-        st.load_q(rows, p.q_scale, tig);
-      }
-      st.reset();
-      for (int c = 0; ok && c < nch; ++c) {
-        const int64_t pos = q + c;
-        const int stage = (int)(pos % kStages);
-        if (!__all_sync(full, mbar_wait(&tail->full[stage], (pos / kStages) & 1, p.err))) {
-          tail->abort = 1;
-          ok = false;
-          break;
-        }
-        if (nrows > 0) {
-          const uint8_t* Ks = ring + stage * G::kStageBytes;
-          st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tail->empty[stage]);
-      }
-      st.finish_sums();
-      if (ok && sg.piece >= p.ws_splits) {
-        if (lane == 0) raise_error(p.err, kErrBounds);
-      } else if (ok) {
-        // the partial of each row: o * v_scale unnormalised, (max, sum) in
-        // log2 units, in split slot `piece` of the member's query head
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-          const int row = grp + 8 * ri;
-          if (row < nrows) {
-            const int member = m0 + row / g;
-            const int64_t wrow =
-                ((int64_t)member * p.Hq + sg.kvh * g + row % g) * p.ws_splits + sg.piece;
-            float* wo = p.ws_o + wrow * D;
-#pragma unroll
-            for (int e = 0; e < 2; ++e)
-#pragma unroll
-              for (int nt = 0; nt < MR::DG; nt += 4)
-                *reinterpret_cast<float4*>(wo + MR::DG * (2 * tig + e) + nt) =
-                    make_float4(st.o[nt][2 * ri + e] * p.v_scale,
-                                st.o[nt + 1][2 * ri + e] * p.v_scale,
-                                st.o[nt + 2][2 * ri + e] * p.v_scale,
-                                st.o[nt + 3][2 * ri + e] * p.v_scale);
-            if (tig == 0) p.ws_ml[wrow] = make_float2(st.m[ri], st.l[ri]);
-          }
-        }
-      }
+      const uint8_t* Ks = ring + stage * G::kStageBytes;
+      st.chunk(Ks, Ks + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(&tail->empty[stage], kConsumerWarps);
+    }
+    st.finish_sums();
+    st.to_comb(comb_o, comb_m, comb_l, warp, g, grp, tig);
+    // one decision for all consumer threads (combine_rows holds a barrier)
+    const bool failed = named_bar_or(1, kConsumerWarps * 32,
+                                     !ok || *reinterpret_cast<volatile int*>(&tail->abort));
+    // the output of a request read in one piece; else its piece's partial
+    const bool direct = sg.n_pieces == 1;
+    if (!direct && sg.piece >= p.ws_splits) {
+      if (tid == 0) raise_error(p.err, kErrBounds);  // device lengths disagree with the plan
+    } else if (!failed) {
+      combine_rows<D>(p, comb_o, comb_m, comb_l, g, sg.r, qs, hq0, direct, sg.piece);
     }
     q += nch;
     // every consumer warp takes the same decision (and the comb buffer is
     // free again for the next unit)
-    if (named_bar_or(2, kConsumerWarps * 32, !ok || *reinterpret_cast<volatile int*>(&tail->abort)))
+    if (named_bar_or(2, kConsumerWarps * 32,
+                     failed || *reinterpret_cast<volatile int*>(&tail->abort)))
       break;
   }
 }
@@ -1262,11 +1177,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeParams p)
     const int32_t* pref = p.pp.aux + 2;
     const int64_t C = pref[r + 1] - pref[r];
     if (C <= 0 || Q <= 0) return;
-    const int kvh = h / p.g;
-    const int64_t a = p.pp.pre_base[p.groups.n] + (int64_t)p.Hkv * pref[r] + kvh * C;
-    const int nt = (int)flat_pieces(a, C, 1, Q);
-    if (grp_id < 0 && nt == 1) return;  // the decode kernel wrote the output
-    nsplit = prefix_pieces_of(p, grp_id, kvh, r, Q) + nt;
+    const int64_t a = (int64_t)p.Hkv * pref[r] + (h / p.g) * C;
+    nsplit = (int)flat_pieces(a, C, Q);  // 1: the decode kernel wrote the output
   } else {
     nsplit = prefix_slots(p.groups, grp_id) + (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
   }

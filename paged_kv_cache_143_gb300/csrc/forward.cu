@@ -190,47 +190,25 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   };
 
   // ---- persistent GQA decode: the decode work as one flat chunk space cut
-  // into equal per-CTA ranges (pa::PersistPlan)
+  // into equal per-CTA ranges (pa::PersistPlan); batches with shared-prefix
+  // groups take the grid kernels (and the prefix pieces on tensor cores)
   pa::PersistPlan pp{};
   int persist_ctas = 0;
-  if (n_dec > 0 && g >= 2 && g <= 16 && R <= pa::kMaxPersistR && ws_splits >= 2 &&
-      gd.n == 0) {
-    const int M = 4 * (16 / g);
-    pp.members_per_block = M;
-    int64_t wp = 0;
-    for (int k = 0; k < gd.n; ++k) {
-      pp.pre_base[k] = (int32_t)wp;
-      const int64_t nblk = (gd.size[k] + M - 1) / M;
-      wp += (int64_t)Hkv * nblk * (gd.prefix_tokens[k] / 16) * pa::kPrefixWeight;
-    }
-    pp.pre_base[gd.n] = (int32_t)wp;
-    int64_t W = wp;
-    for (int r = 0; r < R; ++r) {
-      if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
-      int k_lo;
-      group_slots(r, &k_lo);
-      W += (int64_t)Hkv * ((seq_lens_host[r] - k_lo + 15) / 16);
-    }
-    // slots a request may need with Q units per CTA: the chunk starts of a
-    // unit of C chunks of cost w span w (C - 1) units, so they fall into at
-    // most ceil(w (C - 1) / Q) + 1 CTA ranges (1 if Q >= W)
-    auto unit_slots = [&](int64_t C, int64_t w, int64_t Q) -> int64_t {
-      return Q >= W ? 1 : (w * (C - 1) + Q - 1) / Q + 1;
-    };
+  if (n_dec > 0 && g >= 2 && g <= 16 && R <= pa::kMaxPersistR && ws_splits >= 2 && gd.n == 0) {
+    int64_t W = 0;
+    for (int r = 0; r < R; ++r)
+      if (qsl_host[r + 1] - qsl_host[r] == 1) W += (int64_t)Hkv * ((seq_lens_host[r] + 15) / 16);
+    // slots a request may need with Q chunks per CTA: a unit of C chunks
+    // falls into at most ceil((C - 1) / Q) + 1 CTA ranges (1 if Q >= W)
     auto fits = [&](int64_t Q) {
       for (int r = 0; r < R; ++r) {
         if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
-        int k_lo;
-        group_slots(r, &k_lo);
-        const int k = pa::group_of(gd, r);
-        int64_t need = unit_slots((seq_lens_host[r] - k_lo + 15) / 16, 1, Q);
-        if (k >= 0) need += unit_slots(gd.prefix_tokens[k] / 16, pa::kPrefixWeight, Q);
-        if (need > ws_splits) return false;
+        const int64_t C = (seq_lens_host[r] + 15) / 16;
+        if ((Q >= W ? 1 : (C + Q - 2) / Q + 1) > ws_splits) return false;
       }
       return true;
     };
-    // every CTA range must hold a chunk start: Q >= kPrefixWeight
-    int64_t lo = pa::kPrefixWeight, hi = std::max<int64_t>(W, lo);  // fits(W) holds
+    int64_t lo = 1, hi = std::max<int64_t>(W, 1);  // fits(W) holds: one range
     while (lo < hi) {
       const int64_t mid = (lo + hi) / 2;
       if (fits(mid)) hi = mid; else lo = mid + 1;
@@ -318,8 +296,7 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
       p.ws_ml = ws_ml;
     }
     if (pp.on) {
-      // every decode (tails and the groups' prefixes) in one persistent launch,
-      // then the merge of the pieces
+      // every decode in one persistent launch, then the merge of the pieces
       p.ws_splits = (int)ws_splits;
       p.ws_o = ws_o;
       p.ws_ml = ws_ml;

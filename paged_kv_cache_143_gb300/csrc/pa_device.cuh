@@ -109,6 +109,21 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// 16 bytes global -> shared through L2 only (cp.async.cg), tracked by the
+// executing thread's async-copy groups.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Waits until every async-copy group of this thread has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32). The caller's warp
 // is reconverged first, and the non-aligned form is used, so a warp whose
 // lanes arrive from different branches cannot leave the barrier incomplete.

@@ -38,43 +38,27 @@ __host__ __device__ inline int prefix_slots(const GroupDesc& gd, int grp) {
 }
 
 // ---------------------------------------------------------------------------
-// Persistent GQA decode (2 <= g <= 16). The decode work of one call is laid
-// out as one sequence of cost units, the "flat space"; a 16-key chunk costs
-// one unit when one warp computes it (a decode tail) and kPrefixWeight units
-// when all four consumer warps compute it (a shared prefix, read once for the
-// rows of several members):
-//   [0, W_p)  shared-prefix units: unit (group k, kv head h, member block mb)
-//             holds the group's prefix chunks (C_k = prefix_tokens / 16) and
-//             starts at pre_base[k] + (h * nblk_k + mb) * C_k * kPrefixWeight,
-//             chunk i at kPrefixWeight * i after that, where member block mb
-//             is members [mb * M, mb * M + M) of the group (M =
-//             members_per_block, 4 warps x (16 / g) members) and nblk_k =
-//             ceil(size_k / M);
-//   [W_p, W)  decode tails: unit (request r, kv head h) holds the chunks of
-//             keys [k_lo, seq_len) (k_lo = the group's prefix, or 0) and
-//             starts at W_p + Hkv * pref[r] + h * C_r, pref the exclusive
-//             running sum of C_r over the requests (0 for non-decodes).
-// CTA b of the grid takes the chunks whose start lies in [b Q, b Q + Q),
-// with Q = max(ceil(W / grid), q_min) and q_min >= kPrefixWeight (so every
-// range holds a chunk start). The CTA ranges cut each unit into pieces,
-// piece i being the chunks in CTA floor(a / Q) + i. Every piece writes one
-// partial (split slot): a member's prefix pieces take slots 0 .. n_prefix - 1,
-// its tail pieces the slots after them; an ungrouped request whose tail is
-// one piece writes its output directly.
+// Persistent GQA decode (2 <= g <= 16; batches without shared-prefix groups).
+// The decode work of one call is laid out as one sequence of 16-key chunks,
+// the "flat space": unit (request r, kv head h) holds the chunks of r's keys
+// [0, seq_len) for the g heads of r's token, at Hkv * pref[r] + h * C_r, pref
+// the exclusive running sum of C_r over the requests (0 for non-decodes).
+// CTA b of the grid takes the chunks [b Q, b Q + Q), with
+// Q = max(ceil(W / grid), q_min); the CTA ranges cut each unit [a, a + C)
+// into pieces, piece i being the part in CTA floor(a / Q) + i. A request read
+// in one piece writes its output directly; otherwise every piece writes a
+// partial into split slot i, merged by log-sum-exp.
 constexpr int kMaxPersistR = 512;   // requests the persistent path handles
-constexpr int kPrefixWeight = 4;    // cost units of a shared-prefix chunk
 
 struct PersistPlan {
   int32_t on;                          // 1: decodes run on the persistent kernel
-  int32_t q_min;                       // minimum units per CTA (bounds the slots)
-  int32_t members_per_block;           // M
-  int32_t pre_base[kMaxGroups + 1];    // pre_base[k]: flat start of group k; [n] = W_p
+  int32_t q_min;                       // minimum chunks per CTA (bounds the slots)
   int32_t* aux;                        // workspace: [0] Q, [1] W, [2 + r] pref[r], r <= R
 };
 
-// Pieces of a unit of C chunks of cost w starting at a (chunk i at a + w i).
-__host__ __device__ inline int64_t flat_pieces(int64_t a, int64_t C, int64_t w, int64_t Q) {
-  return C <= 0 ? 0 : (a + w * (C - 1)) / Q - a / Q + 1;
+// Pieces of a unit of C chunks starting at a, for ranges of Q chunks.
+__host__ __device__ inline int64_t flat_pieces(int64_t a, int64_t C, int64_t Q) {
+  return C <= 0 ? 0 : (a + C - 1) / Q - a / Q + 1;
 }
 
 // Words of the persistent plan's area at the start of the workspace.
@@ -110,20 +94,6 @@ struct DecodeParams {
   int32_t R;                   // requests
   PersistPlan pp;              // the persistent kernel's plan (pp.on == 0: grid kernels)
 };
-
-// Persistent plan: the pieces of the shared-prefix unit that holds member r
-// of group grp at kv head h (0 if grp < 0), for chunks per CTA Q. They take
-// the member's first split slots.
-__host__ __device__ inline int prefix_pieces_of(const DecodeParams& p, int grp, int h, int r,
-                                                int64_t Q) {
-  if (grp < 0) return 0;
-  const int Mb = p.pp.members_per_block;
-  const int64_t nblk = (p.groups.size[grp] + Mb - 1) / Mb;
-  const int64_t mb = (r - p.groups.first[grp]) / Mb;
-  const int64_t C = p.groups.prefix_tokens[grp] / 16;
-  const int64_t a = p.pp.pre_base[grp] + ((int64_t)h * nblk + mb) * C * kPrefixWeight;
-  return (int)flat_pieces(a, C, kPrefixWeight, Q);
-}
 
 constexpr int kMaxOrderedPrefill = 256;
 
