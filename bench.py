@@ -412,6 +412,37 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
     }
 
 
+def run_prefill_only(args, dev, cfg, kv_dtype=None, n_chunks=None):
+    """The prefill chunks of config `cfg` alone (the first n_chunks of them):
+    pa_forward on the chunks' step, causal TFLOP/s (a narrow command for
+    profiler captures of the tensor-core prefill kernel)."""
+    import torch
+    import workloads
+    from paged_kv_cache_143_gb300 import accounting, pa
+    w = workloads.make(cfg, device=dev, kv_dtype=kv_dtype)
+    ql = np.diff(w.qsl)
+    chunks = np.nonzero(ql > 1)[0][:n_chunks]
+    seq, name = w.seq_lens[chunks], w.name
+    Hq, Hkv, D, B, kvd = w.Hq, w.Hkv, w.D, w.B, w.kv_dtype
+    pairs = sum(accounting.causal_pairs(int(ql[r]), int(w.seq_lens[r])) for r in chunks)
+    flops = accounting.attention_flops(pairs, Hq, D)
+    del w
+    torch.cuda.empty_cache()
+    wp = workloads.build(seq, ql[chunks], Hq, Hkv, D, B, kv_dtype=kvd,
+                         seed=workloads.config_seed(cfg, 1), device=dev)
+    sp = Step(wp, dev, max_splits=32)
+    sp.run()
+    fwd = lambda: pa.forward(sp.q, sp.out, sp.qsl, sp.seq, wp.qsl, wp.seq_lens, sp.gathered,
+                             sp.pool, wp.scale, wp.causal, workspace=sp.ws)
+    ms = timed(fwd, args.steps, args.warmup, torch.cuda.current_stream())
+    if pa.get_error() != pa.PA_OK:
+        raise RuntimeError("device error in the prefill chunks")
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": f"{name} prefill chunks x{len(chunks)}", "ms": round(ms, 4),
+            "causal_flops": int(flops), "tflops": round(tf, 1),
+            "frac": round(tf / load_peaks_tensor(), 4)}
+
+
 def run_prefix_shared(args, dev):
     """Prefix-shared parallel sampling (8 groups x 16 samples, FP8 KV): decode
     step time, logical KV bytes (what every request reads) and unique KV bytes
@@ -774,8 +805,12 @@ def main():
                          "are for profiling captures)")
     ap.add_argument("--no-cpu", dest="cpu_legs", action="store_false",
                     help="skip the oracle timings on the host cores (profiling runs)")
+    ap.add_argument("--chunks", type=int, default=None,
+                    help="prefill-long: how many of the long-context prefill chunks to run")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="prefill-long: KV cache element type")
     ap.add_argument("--only", choices=["decode", "mixed", "long-bf16", "long-fp8",
-                                       "prefix-shared", "tiny", "serving"],
+                                       "prefill-long", "prefix-shared", "tiny", "serving"],
                     default=None,
                     help="run one workload alone (the benchmark's decode batch or a "
                          "secondary workload) and print its object (a narrow command for "
@@ -791,6 +826,7 @@ def main():
                "mixed": lambda: run_mixed(args, dev, 3),
                "long-bf16": lambda: run_mixed(args, dev, 5, "bf16"),
                "long-fp8": lambda: run_mixed(args, dev, 5, "fp8"),
+               "prefill-long": lambda: run_prefill_only(args, dev, 5, args.kv, args.chunks),
                "prefix-shared": lambda: run_prefix_shared(args, dev),
                "tiny": lambda: run_tiny(args, dev),
                "serving": lambda: run_serving(args, dev)}[args.only]
