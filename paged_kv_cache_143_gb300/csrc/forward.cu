@@ -92,7 +92,6 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     }
   }
   if (R > 65535) return PA_ERR_UNSUPPORTED;
-  if (g > 128 && cas && cas->n > 0) return PA_ERR_UNSUPPORTED;  // prefix tiles, as above
 
   // ---- shared-prefix groups: consecutive decode requests, each with keys
   // past the prefix
@@ -123,16 +122,13 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   const int64_t ws_splits = row_bytes ? (int64_t)(part_bytes / row_bytes) : 0;
   // the pieces of a prefix and at least one tail split each need a slot
   if (gd.n > 0 && ws_splits < 2) return PA_ERR_INVALID;
-  int pieces = 0, pairs_per_piece = 0;
+  int pieces = 0;
   if (gd.n > 0) {
-    // enough prefix CTAs to fill the GPU once, each piece at least 512 keys
-    const int tiles = (max_members + 128 / g - 1) / (128 / g);
-    pairs_per_piece = (tiles + 1) / 2;
-    const int64_t ctas = (int64_t)gd.n * Hkv * pairs_per_piece;
-    int64_t want = std::max<int64_t>(1, pa::num_sms() / ctas);
-    want = std::min<int64_t>(want, (max_prefix + 511) / 512);
-    want = std::min<int64_t>(want, ws_splits - 1);
-    gd.prefix_split_tokens = round_up((int)((max_prefix + want - 1) / want), 128);
+    // prefix pieces of 512 keys (32 chunks: a ring and a half of stages per
+    // CTA), fewer and longer when the workspace's slots run out: a member
+    // needs one slot per piece and at least one for its tail
+    const int64_t want = (max_prefix + ws_splits - 2) / (ws_splits - 1);
+    gd.prefix_split_tokens = round_up((int)std::max<int64_t>(512, want), 16);
     pieces = (max_prefix + gd.prefix_split_tokens - 1) / gd.prefix_split_tokens;
   }
   // decode key range of request r: [k_lo, seq)
@@ -249,53 +245,45 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
     p.R = R;
     p.pp = pp;
 
-    // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
-    // least 256 keys, a multiple of the 16-key chunk; bounded by the slots
-    // the workspace holds (a group member's prefix pieces take the first
-    // ones). Depends only on seq_lens and the groups, never on placement.
-    const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
-    int64_t split = (dec_keys * Hkv * p.head_groups + target_ctas - 1) / target_ctas;
-    split = std::max<int64_t>(split, 256);
-    split = std::min<int64_t>(split, max_dec_len);
-    split = round_up((int)split, 16);
-    auto plan = [&](int64_t sp, int* grid_x) {
-      int need = 0, gx = 0;
+    if (gd.n > 0) {
+      // shared-prefix batch: the groups' prefix pieces and every decode's keys
+      // after its prefix in one launch (cascade.cu), then the merge. Tail
+      // splits of at least 256 keys, few enough for the slots left after a
+      // member's prefix pieces.
+      int64_t sp = 256;
       for (int r = 0; r < R; ++r) {
         if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
         int k_lo;
-        const int slot0 = group_slots(r, &k_lo);
-        const int n = (int)((seq_lens_host[r] - k_lo + sp - 1) / sp);
-        gx = std::max(gx, n);
-        need = std::max(need, slot0 + n);
+        const int free_slots = (int)ws_splits - group_slots(r, &k_lo);
+        sp = std::max<int64_t>(sp, (seq_lens_host[r] - k_lo + free_slots - 1) / free_slots);
       }
-      *grid_x = gx;
-      return need;
-    };
-    int grid_x;
-    int need = plan(split, &grid_x);
-    if (need > 1 && need > ws_splits) {
-      if (ws_splits <= 1) {  // no groups here: one split per request, no workspace
-        split = round_up(max_dec_len, 16);
-      } else {
-        int64_t sp = 16;
-        for (int r = 0; r < R; ++r) {
-          if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
-          int k_lo;
-          const int free_slots = (int)ws_splits - group_slots(r, &k_lo);
-          sp = std::max<int64_t>(sp, (seq_lens_host[r] - k_lo + free_slots - 1) / free_slots);
-        }
-        split = round_up((int)sp, 16);
+      sp = round_up((int)sp, 16);
+      const int units = Hkv * p.head_groups;
+      int64_t tail_ctas = 1;
+      for (int r = 0; r < R; ++r) {
+        if (qsl_host[r + 1] - qsl_host[r] != 1) continue;
+        int k_lo;
+        group_slots(r, &k_lo);
+        const int64_t ns = (seq_lens_host[r] - k_lo + sp - 1) / sp;
+        tail_ctas = std::max<int64_t>(tail_ctas, (ns * units + 3) / 4);
       }
-      need = plan(split, &grid_x);
-    }
-    if (grid_x > 65535) return PA_ERR_UNSUPPORTED;
-    p.split_tokens = (int)split;
-    p.ws_splits = need > 1 ? (int)ws_splits : 1;
-    if (need > 1) {
+      pa::CascadePlan cp{};
+      cp.pieces = pieces;
+      cp.row_blocks = (int)(((int64_t)max_members * g + 63) / 64);
+      const int64_t n_pref = (int64_t)gd.n * pieces * Hkv * cp.row_blocks;
+      if (n_pref + (int64_t)R * tail_ctas > INT32_MAX) return PA_ERR_UNSUPPORTED;
+      cp.n_prefix_ctas = (int32_t)n_pref;
+      cp.tail_ctas = (int32_t)tail_ctas;
+      p.split_tokens = (int)sp;
+      p.ws_splits = (int)ws_splits;
       p.ws_o = ws_o;
       p.ws_ml = ws_ml;
-    }
-    if (pp.on) {
+      if (pa::launch_cascade(p, cp, D, fp8, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+      // every group member has a prefix partial and a tail partial
+      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+      pa::count_launches(1);
+    } else if (pp.on) {
       // every decode in one persistent launch, then the merge of the pieces
       p.ws_splits = (int)ws_splits;
       p.ws_o = ws_o;
@@ -305,26 +293,45 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
       if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
       pa::count_launches(1);
     } else {
-    if (gd.n > 0) {  // the prefix pieces of every group, into slots 0..pieces-1
-      pa::PrefillLaunch L = prefill_launch();
-      L.p.mode = 1;
-      L.p.causal = 0;
-      L.p.groups = gd;
-      L.p.pairs_per_piece = pairs_per_piece;
-      L.p.ws_o = ws_o;
-      L.p.ws_ml = ws_ml;
-      L.p.ws_splits = (int)ws_splits;
-      L.max_q_tiles = 2 * pairs_per_piece;
-      L.pieces = pieces;
-      if (pa::launch_prefill(L, s) != cudaSuccess) return PA_ERR_CUDA;
+      // Split size: enough CTAs for ~4 waves of 2 CTAs per SM, each split at
+      // least 256 keys, a multiple of the 16-key chunk; bounded by the slots
+      // the workspace holds. Depends only on seq_lens, never on placement.
+      const int64_t target_ctas = (int64_t)pa::num_sms() * 2 * 4;
+      int64_t split = (dec_keys * Hkv * p.head_groups + target_ctas - 1) / target_ctas;
+      split = std::max<int64_t>(split, 256);
+      split = std::min<int64_t>(split, max_dec_len);
+      split = round_up((int)split, 16);
+      auto plan = [&](int64_t sp, int* grid_x) {
+        int gx = 0;
+        for (int r = 0; r < R; ++r)
+          if (qsl_host[r + 1] - qsl_host[r] == 1)
+            gx = std::max(gx, (int)((seq_lens_host[r] + sp - 1) / sp));
+        *grid_x = gx;
+        return gx;  // split slots a request needs
+      };
+      int grid_x;
+      int need = plan(split, &grid_x);
+      if (need > 1 && need > ws_splits) {
+        if (ws_splits <= 1) {  // no groups here: one split per request, no workspace
+          split = round_up(max_dec_len, 16);
+        } else {
+          split = round_up((int)((max_dec_len + ws_splits - 1) / ws_splits), 16);
+        }
+        need = plan(split, &grid_x);
+      }
+      if (grid_x > 65535) return PA_ERR_UNSUPPORTED;
+      p.split_tokens = (int)split;
+      p.ws_splits = need > 1 ? (int)ws_splits : 1;
+      if (need > 1) {
+        p.ws_o = ws_o;
+        p.ws_ml = ws_ml;
+      }
+      if (pa::launch_decode(p, D, fp8, R, grid_x, s) != cudaSuccess) return PA_ERR_CUDA;
       pa::count_launches(1);
-    }
-    if (pa::launch_decode(p, D, fp8, R, grid_x, s) != cudaSuccess) return PA_ERR_CUDA;
-    pa::count_launches(1);
-    if (need > 1) {
-      if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
-      pa::count_launches(1);
-    }
+      if (need > 1) {
+        if (pa::launch_merge(p, D, R, s) != cudaSuccess) return PA_ERR_CUDA;
+        pa::count_launches(1);
+      }
     }
   }
 

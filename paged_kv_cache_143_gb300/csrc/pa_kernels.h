@@ -15,7 +15,7 @@ struct GroupDesc {
   int32_t first[kMaxGroups];          // group k = requests [first[k], first[k] + size[k]),
   int32_t size[kMaxGroups];           //   increasing and disjoint
   int32_t prefix_tokens[kMaxGroups];  // shared prefix length (whole blocks)
-  // the prefix is cut into pieces of this many keys (a multiple of 128);
+  // the prefix is cut into pieces of this many keys (a multiple of 16);
   // piece i of a member's prefix lands in split slot i, its tail after them
   int32_t prefix_split_tokens;
 };
@@ -114,16 +114,6 @@ struct PrefillParams {
   // grid.z walks every request in batch order
   int32_t n_order;
   int32_t order[kMaxOrderedPrefill];
-  // mode 1: the CTAs of blockIdx.z = k attend the decode tokens of group k's
-  // members (consecutive tokens) to its shared prefix [0, prefix_tokens),
-  // non-causally, and write fp32 partials (o, max, sum) into slot 0 of the
-  // decode workspace instead of bf16 output
-  int32_t mode;
-  int32_t pairs_per_piece;  // mode 1: blockIdx.x = piece * pairs_per_piece + tile pair
-  GroupDesc groups;
-  float* ws_o;
-  float2* ws_ml;
-  int32_t ws_splits;
 };
 
 struct PrefillLaunch {
@@ -133,11 +123,28 @@ struct PrefillLaunch {
   const void* v_pool;
   int32_t T, R, D;
   bool fp8;                    // E4M3 pools
-  int32_t max_q_tiles;         // max over prefill requests of ceil(q_len * g / 128)
-  int32_t pieces;              // mode 1: prefix pieces per group (grid x = pieces * pairs)
+  int32_t max_q_tiles;         // max over prefill requests of ceil(q_len / (128 / g))
 };
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t s);
+
+// Grid of the shared-prefix decode (cascade.cu): n_prefix_ctas CTAs for the
+// groups' prefixes, laid out as [group][piece][kv head][row block] (a row
+// block = 64 of the group's (member, head) rows, member-major), then
+// tail_ctas CTAs per request, each taking four (key split, kv head, 16-head
+// part) tasks of the request.
+struct CascadePlan {
+  int32_t n_prefix_ctas;
+  int32_t pieces;       // prefix pieces per group (of groups.prefix_split_tokens keys)
+  int32_t row_blocks;   // row blocks per (group, piece, kv head)
+  int32_t tail_ctas;    // CTAs per request
+};
+// Prefix pieces and private tails of a batch with shared-prefix groups, into
+// the split slots of the workspace (p.ws_o, p.ws_ml): a member's prefix
+// piece i in slot i, its tail splits after them; an ungrouped request read
+// in one split writes its bf16 output directly.
+cudaError_t launch_cascade(const DecodeParams& p, const CascadePlan& cp, int D, bool fp8,
+                           cudaStream_t s);
 
 cudaError_t launch_decode(const DecodeParams& p, int D, bool fp8, int R, int max_splits,
                           cudaStream_t s);

@@ -158,45 +158,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + S::kOffBar);
 
-  // mode 0: a prefill chunk of request r. Mode 1: the decode tokens of the
-  // members of group blockIdx.z (consecutive requests, one token each) against
-  // one piece of their shared prefix, as a virtual non-causal chunk whose key
-  // range is the piece (the block table of the first member, from the piece on).
-  int r, q_begin, q_len, seq, piece = 0, pair_x = blockIdx.x;
-  const int32_t* table;
-  if (p.mode == 1) {
-    const int grp = blockIdx.z;
-    piece = (int)blockIdx.x / p.pairs_per_piece;
-    pair_x = (int)blockIdx.x % p.pairs_per_piece;
-    r = p.groups.first[grp];
-    q_begin = p.qsl[r];
-    q_len = p.groups.size[grp];
-    if (p.qsl[r + q_len] - q_begin != q_len || q_begin < 0 || q_begin + q_len > p.T) {
-      // members are not all decodes, or a device qsl leaves q
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    const int k_first = piece * p.groups.prefix_split_tokens;
-    if (k_first >= p.groups.prefix_tokens[grp]) return;
-    seq = min(p.groups.prefix_tokens[grp] - k_first, p.groups.prefix_split_tokens);
-    table = p.block_tables + (int64_t)r * p.max_blocks + k_first / p.B;
-  } else {
-    r = p.n_order ? p.order[blockIdx.z] : (int)blockIdx.z;
-    q_begin = p.qsl[r];
-    q_len = p.qsl[r + 1] - q_begin;
-    if (q_len <= 1) return;  // decode requests and empty requests are not ours
-    seq = p.seq_lens[r];
-    if (seq < q_len || seq > p.max_blocks * p.B || q_begin < 0 || q_begin + q_len > p.T) {
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    table = p.block_tables + (int64_t)r * p.max_blocks;
+  // a prefill chunk of request r (grid z: the requests, heaviest first)
+  const int r = p.n_order ? p.order[blockIdx.z] : (int)blockIdx.z;
+  const int q_begin = p.qsl[r];
+  const int q_len = p.qsl[r + 1] - q_begin;
+  if (q_len <= 1) return;  // decode requests and empty requests are not ours
+  const int seq = p.seq_lens[r];
+  if (seq < q_len || seq > p.max_blocks * p.B || q_begin < 0 || q_begin + q_len > p.T) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    return;
   }
+  const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
+  const int pair_x = blockIdx.x;
   const int g = p.g;
   const int tpt = kM / g;  // tokens per tile
   const int ntq = (q_len + tpt - 1) / tpt;
   const int npairs = (ntq + 1) / 2;
-  if (npairs > (p.mode == 1 ? p.pairs_per_piece : (int)gridDim.x)) {
+  if (npairs > (int)gridDim.x) {
     // more query tiles than the grid was planned for: device qsl disagrees
     // with the host mirror; the tiles past the grid would be left unwritten
     if (threadIdx.x == 0 && pair_x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
@@ -204,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (pair_x >= npairs) return;
   const int pair = npairs - 1 - pair_x;  // heaviest (latest) pairs start first
   const int kvh = blockIdx.y;
-  const int P = p.mode == 1 ? 0 : seq - q_len;
+  const int P = seq - q_len;
   int q0[2], ntk[2], n_kv[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
@@ -757,29 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         !__all_sync(0xffffffffu, mbar_wait(&bars->pv_done[t], (my_ntk - 1) & 1, p.err)))
       ok = false;
     if (!ok) bars->abort = 1;
-    if (ok && my_ntk > 0 && !aborted(bars) && p.mode == 1) {
-      // partial of this prefix piece: o * v_scale unnormalised, (max, sum) in
-      // log2 units, in split slot `piece` of the member request
-      tc::fence_after_sync();
-      const int64_t wrow = ((int64_t)(r + tok) * p.Hq + kvh * g + head) * p.ws_splits + piece;
-      float* wo = p.ws_o + wrow * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tc::tmem_ld32(tmem_o + c * 32, o);
-        tc::tmem_wait_ld();
-        if (valid_row) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(wo + c * 32 + q * 4) =
-                make_float4(__uint_as_float(o[4 * q]) * p.v_scale,
-                            __uint_as_float(o[4 * q + 1]) * p.v_scale,
-                            __uint_as_float(o[4 * q + 2]) * p.v_scale,
-                            __uint_as_float(o[4 * q + 3]) * p.v_scale);
-        }
-      }
-      if (valid_row) p.ws_ml[wrow] = make_float2(m_run, l_run);
-    } else if (ok && my_ntk > 0 && !aborted(bars)) {
+    if (ok && my_ntk > 0 && !aborted(bars)) {
       tc::fence_after_sync();
       const float inv_l = l_run > 0.f ? p.v_scale / l_run : 0.f;
       __nv_bfloat16* orow = p.out + ((int64_t)(q_begin + tok) * p.Hq + kvh * g + head) * D;
@@ -863,9 +819,8 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   e = cudaFuncGetAttributes(&fa, prefill_kernel<D, F8>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
-  // tile pairs (x pieces of the prefix in mode 1)
-  dim3 grid(p.mode == 1 ? p.pairs_per_piece * L.pieces : (L.max_q_tiles + 1) / 2, p.Hkv,
-            p.mode == 1 ? p.groups.n : (p.n_order ? p.n_order : L.R));
+  // tile pairs x kv heads x prefill requests
+  dim3 grid((L.max_q_tiles + 1) / 2, p.Hkv, p.n_order ? p.n_order : L.R);
   prefill_kernel<D, F8><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
