@@ -11,10 +11,11 @@
 // member's decode token can be computed against one read of the prefix.
 //
 // Both kinds of CTA are four warps; each warp owns up to 16 query rows and
-// runs the warp-level tensor-core decode (MmaRows: mma.sync m16n8k16, S and
-// P.V per 16-key chunk, two chunks per online-softmax update, everything in
-// registers). Nothing is combined across warps: a warp writes its rows'
-// partial (or final) output itself.
+// runs the warp-level tensor-core decode (decode_rows.cuh: mma.sync
+// m16n8k16, S and P.V per 16-key chunk, two chunks per online-softmax
+// update, everything in registers; tails of GQA groups of at most 8 heads
+// of E4M3 pools with the keys as the MMA rows). Nothing is combined across warps: a warp
+// writes its rows' partial (or final) output itself.
 //  - prefix CTA (group k, piece, kv head, row block): rows = (member, head)
 //    pairs of the group, 64 per CTA (16 per warp), against one piece of the
 //    prefix read through the first member's table row. The four warps share
@@ -104,175 +105,73 @@ __device__ __forceinline__ void issue_chunk(const DecodeParams& p, uint8_t* ring
   }
 }
 
-// Writes a warp's rows grp and grp + 8: the final bf16 output (direct) or
-// the fp32 partial (o * v_scale, max, sum) into split slot `slot`. Row ri is
-// request req[ri] (query token qtok[ri]), query head hq[ri]; rows that are
-// not live are padding.
-template <int D, bool FP8>
-__device__ __forceinline__ void write_rows(const DecodeParams& p, const MmaRows<D, FP8>& st,
-                                           const int (&req)[2], const int (&qtok)[2],
-                                           const int (&hq)[2], const bool (&live)[2],
-                                           bool direct, int slot, int tig) {
-  constexpr int DG = MmaRows<D, FP8>::DG;
-#pragma unroll
-  for (int ri = 0; ri < 2; ++ri) {
-    if (!live[ri]) continue;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int d0 = DG * (2 * tig + e);  // dims d0 .. d0 + DG - 1 (o[nt][2 ri + e], nt = dim)
-      if (direct) {
-        const float f = p.v_scale / st.l[ri];
-        uint32_t w[DG / 2];
-#pragma unroll
-        for (int i = 0; i < DG / 2; ++i) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(st.o[2 * i][2 * ri + e] * f,
-                                                         st.o[2 * i + 1][2 * ri + e] * f);
-          w[i] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        uint4* o = reinterpret_cast<uint4*>(p.out + ((int64_t)qtok[ri] * p.Hq + hq[ri]) * D + d0);
-#pragma unroll
-        for (int i = 0; i < DG / 8; ++i)
-          o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      } else {
-        const int64_t orow = ((int64_t)req[ri] * p.Hq + hq[ri]) * p.ws_splits + slot;
-        float4* o = reinterpret_cast<float4*>(p.ws_o + orow * D + d0);
-        const float v = p.v_scale;
-#pragma unroll
-        for (int i = 0; i < DG / 4; ++i)
-          o[i] = make_float4(st.o[4 * i][2 * ri + e] * v, st.o[4 * i + 1][2 * ri + e] * v,
-                             st.o[4 * i + 2][2 * ri + e] * v, st.o[4 * i + 3][2 * ri + e] * v);
-        if (tig == 0 && e == 0) p.ws_ml[orow] = make_float2(st.m[ri], st.l[ri]);
-      }
+// Where a warp's rows go: row i (< 16) of the warp is a (request, query
+// token, query head), or padding.
+struct WarpRows {
+  int nrows;  // rows of the warp (0: none)
+  // prefix CTA: (member, head) row r0 + i of the group of `first` (query
+  // tokens from q_begin on), heads of kv head kvh; tail CTA: query head
+  // hq0 + i of request `req` (query token qtok)
+  bool prefix;
+  int r0, first, q_begin, kvh;
+  int req, qtok, hq0;
+  __device__ __forceinline__ bool get(int g, int i, int& r, int& qt, int& hq) const {
+    if (i >= nrows) return false;
+    if (prefix) {
+      const int gr = r0 + i, mem = gr / g;
+      r = first + mem;
+      qt = q_begin + mem;
+      hq = kvh * g + gr % g;
+    } else {
+      r = req;
+      qt = qtok;
+      hq = hq0 + i;
     }
+    return true;
   }
-}
+};
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kCThreads, 3)
-    cascade_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                          const __grid_constant__ CUtensorMap tmap_v, DecodeParams p,
-                          CascadePlan cp) {
-  using G = Geo<D, FP8>;
-  using CG = CascadeGeo<D, FP8>;
-  using MR = MmaRows<D, FP8>;
-  constexpr int S = CG::kStages;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* ring = smem;
-  if constexpr (CG::kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;  // 1024-byte aligned
-  CascadeSmem* cs = reinterpret_cast<CascadeSmem*>(ring + S * G::kStageBytes);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int grp = lane >> 2, tig = lane & 3;
-  const unsigned full = 0xffffffffu;
-  const bool prefix = (int)blockIdx.x < cp.n_prefix_ctas;
-
-  // ---- this warp's rows, key run and destination
+// One warp's key run and its rows: the chunks [0, nch) of keys k_begin + 16 c
+// (masked at k_end) of kv head kvh through `table`, in the stages
+// stage0 + (c mod sw) of the ring; a prefix CTA's warps share the ring (nact
+// of them consume every chunk), a tail warp owns its sw stages.
+struct WarpJob {
   const int32_t* table;
   int kvh, k_begin, k_end, nch, nact, sw, stage0, slot;
-  bool direct = false;
-  int req[2], qtok[2], hq[2];
-  bool live[2];
-  if (prefix) {
-    int b = blockIdx.x;
-    const int rb = b % cp.row_blocks;
-    b /= cp.row_blocks;
-    kvh = b % p.Hkv;
-    b /= p.Hkv;
-    const int piece = b % cp.pieces;
-    const int k = b / cp.pieces;
-    if (k >= p.groups.n) return;
-    const int first = p.groups.first[k], n = p.groups.size[k];
-    const int q_begin = p.qsl[first];
-    if (p.qsl[first + n] - q_begin != n || q_begin < 0 || q_begin + n > p.T) {
-      // members are not all decodes, or a device qsl leaves q / out
-      if (threadIdx.x == 0 && rb == 0 && kvh == 0 && piece == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    k_begin = piece * p.groups.prefix_split_tokens;
-    if (k_begin >= p.groups.prefix_tokens[k]) return;
-    k_end = min(p.groups.prefix_tokens[k], k_begin + p.groups.prefix_split_tokens);
-    const int rows = n * p.g;  // (member, head) rows of the group
-    const int row0 = rb * kRowsPerCta;
-    if (row0 >= rows) return;
-    nact = min(kCWarps, (rows - row0 + 15) / 16);
-    table = p.block_tables + (int64_t)first * p.max_blocks;
-    sw = S;
-    stage0 = 0;
-    slot = piece;
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-      const int gr = row0 + warp * 16 + grp + 8 * ri;
-      live[ri] = gr < rows;
-      const int m = live[ri] ? gr / p.g : 0;
-      req[ri] = first + m;
-      qtok[ri] = q_begin + m;
-      hq[ri] = kvh * p.g + (live[ri] ? gr % p.g : 0);
-    }
-    // a warp without rows only takes part in the barriers
-    nch = warp < nact ? (k_end - k_begin + kChunk - 1) / kChunk : 0;
-  } else {
-    const int b = (int)blockIdx.x - cp.n_prefix_ctas;
-    const int r = b / cp.tail_ctas, x = b % cp.tail_ctas;
-    if (r >= p.R) return;
-    const int qs = p.qsl[r];
-    if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
-    const int seq = p.seq_lens[r];
-    if (qs < 0 || qs >= p.T || seq < 1 || seq > p.max_blocks * p.B) {
-      if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    const int grp_id = group_of(p.groups, r);
-    const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
-    const int slot0 = prefix_slots(p.groups, grp_id);
-    if (k_lo >= seq) {
-      if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
-    const int units = p.Hkv * p.head_groups;  // (kv head, 16-head part) of a split
-    if ((int64_t)nsplit * units > (int64_t)cp.tail_ctas * kCWarps ||
-        (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
-      // device seq_lens disagree with the host mirror the grid was planned from
-      if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
-      return;
-    }
-    if (x * kCWarps >= nsplit * units) return;
-    const int t = x * kCWarps + warp;
-    const int split = t / units, u = t % units;
-    kvh = u / p.head_groups;
-    const int part = u % p.head_groups;
-    const int hq0 = kvh * p.g + 16 * part;
-    const int nrows = t < nsplit * units ? min(16, p.g - 16 * part) : 0;
-    k_begin = k_lo + split * p.split_tokens;
-    k_end = min(seq, k_begin + p.split_tokens);
-    nch = nrows > 0 ? (k_end - k_begin + kChunk - 1) / kChunk : 0;
-    table = p.block_tables + (int64_t)r * p.max_blocks;
-    nact = 1;
-    sw = CG::kTailStages;
-    stage0 = warp * CG::kTailStages;
-    direct = slot0 + nsplit == 1;
-    slot = slot0 + split;
-#pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-      live[ri] = grp + 8 * ri < nrows;
-      req[ri] = r;
-      qtok[ri] = qs;
-      hq[ri] = hq0 + grp + 8 * ri;
-    }
-  }
+  bool prefix, direct, fills;
+  WarpRows rows;
+};
+
+// The body of the kernel for one row-state type (MmaRows: up to 16 query
+// rows; MmaKeys: up to 8 heads, keys as the MMA rows): start-up, streaming
+// of the warp's key run, output.
+template <int D, bool FP8, class RS>
+__device__ __forceinline__ void cascade_warp(const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
+                                             const DecodeParams& p, uint8_t* ring,
+                                             CascadeSmem* cs, const WarpJob& jb) {
+  using G = Geo<D, FP8>;
+  constexpr int S = CascadeGeo<D, FP8>::kStages;
+  const int lane = threadIdx.x & 31;
+  const int grp = lane >> 2, tig = lane & 3;
+  const unsigned full = 0xffffffffu;
+  const int nch = jb.nch, sw = jb.sw, stage0 = jb.stage0;
 
   // start-up: the query rows and the first block ids are requested before
   // the barriers are set up, so that their latencies overlap
   IdWindow win;
-  const bool fills = prefix ? warp == 0 : nch > 0;
-  typename MR::QRaw qraw;
+  typename RS::QRaw qraw;
   if (nch > 0) {
     const __nv_bfloat16* rows[2];
 #pragma unroll
-    for (int ri = 0; ri < 2; ++ri)
-      rows[ri] = live[ri] ? p.q + ((int64_t)qtok[ri] * p.Hq + hq[ri]) * D : nullptr;
-    MR::fetch_q(rows, qraw, tig);
+    for (int ri = 0; ri < 2; ++ri) {
+      int r, qt, hq;
+      rows[ri] = jb.rows.get(p.g, grp + 8 * ri, r, qt, hq)
+                     ? p.q + ((int64_t)qt * p.Hq + hq) * D
+                     : nullptr;
+    }
+    RS::fetch_q(rows, qraw, tig);
   }
-  if (fills && nch > 0) win.get(p, table, k_begin, nch, 0, lane);  // lane i: the id of chunk i
+  if (jb.fills && nch > 0) win.get(p, jb.table, jb.k_begin, nch, 0, lane);  // lane i: chunk i
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&cs->full[i], 1);
@@ -286,21 +185,21 @@ __global__ void __launch_bounds__(kCThreads, 3)
 
   // ---- the first stages: a prefix CTA's ring filled by warp 0, a tail
   // warp's quarter by the warp itself (lane i: chunk i)
-  if (fills && nch > 0) {
-    if (CG::kSw && lane == 0) {
-      tc::prefetch_tensormap(&tmap_k);
-      tc::prefetch_tensormap(&tmap_v);
+  if (jb.fills && nch > 0) {
+    if (CascadeGeo<D, FP8>::kSw && lane == 0) {
+      tc::prefetch_tensormap(tmap_k);
+      tc::prefetch_tensormap(tmap_v);
     }
     const int n0 = min(sw, nch);
     if (lane < n0)
-      issue_chunk<D, FP8>(p, ring, cs, &tmap_k, &tmap_v, stage0 + lane, kvh,
-                          k_begin + lane * kChunk, win.id);
-    if (prefix && lane == 0) cs->issued = n0;
+      issue_chunk<D, FP8>(p, ring, cs, tmap_k, tmap_v, stage0 + lane, jb.kvh,
+                          jb.k_begin + lane * kChunk, win.id);
+    if (jb.prefix && lane == 0) cs->issued = n0;
   }
 
-  MR st;
+  RS st;
   bool ok = true;
-  int consumed = 0, issued_w = fills ? min(sw, nch) : 0;  // tail warps: own accounting
+  int consumed = 0, issued_w = jb.fills ? min(sw, nch) : 0;  // tail warps: own accounting
   if (nch > 0) {
     st.load_q(qraw, p.q_scale, tig);
     st.reset();
@@ -321,9 +220,9 @@ __global__ void __launch_bounds__(kCThreads, 3)
         const uint8_t* K1 = ring + st1 * G::kStageBytes;
         const uint8_t* const ks[2] = {K0, K1};
         const uint8_t* const vs[2] = {K0 + G::kChunkBytes, K1 + G::kChunkBytes};
-        st.template chunks<2>(ks, vs, k_begin + c * kChunk, k_end, grp, tig);
+        st.template chunks<2>(ks, vs, jb.k_begin + c * kChunk, jb.k_end, grp, tig);
       } else {
-        st.chunk(K0, K0 + G::kChunkBytes, k_begin + c * kChunk, k_end, grp, tig);
+        st.chunk(K0, K0 + G::kChunkBytes, jb.k_begin + c * kChunk, jb.k_end, grp, tig);
       }
       consumed = c + n;
       // each stage takes the chunk one ring ahead next, issued by the last
@@ -331,23 +230,23 @@ __global__ void __launch_bounds__(kCThreads, 3)
       // their values are in registers, consumed by MMAs already issued)
       for (int i = 0; i < n; ++i) {
         const int cc = c + i, stage = stage0 + cc % sw, cn = cc + sw;
-        const int id = cn < nch ? win.get(p, table, k_begin, nch, cn, lane) : 0;
+        const int id = cn < nch ? win.get(p, jb.table, jb.k_begin, nch, cn, lane) : 0;
         __syncwarp();
         bool last = true;
-        if (prefix && cn < nch) {
+        if (jb.prefix && cn < nch) {
           int old = 0;
           if (lane == 0) {
             __threadfence_block();
             old = atomicAdd(&cs->done[stage], 1);
           }
-          last = (__shfl_sync(full, old, 0) + 1) % nact == 0;
+          last = (__shfl_sync(full, old, 0) + 1) % jb.nact == 0;
         }
         if (last && cn < nch) {
           if (lane == 0) {
             __threadfence_block();
-            issue_chunk<D, FP8>(p, ring, cs, &tmap_k, &tmap_v, stage, kvh,
-                                k_begin + cn * kChunk, id);
-            if (prefix) atomicMax(&cs->issued, cn + 1);
+            issue_chunk<D, FP8>(p, ring, cs, tmap_k, tmap_v, stage, jb.kvh,
+                                jb.k_begin + cn * kChunk, id);
+            if (jb.prefix) atomicMax(&cs->issued, cn + 1);
           }
           issued_w = cn + 1;
         }
@@ -355,12 +254,36 @@ __global__ void __launch_bounds__(kCThreads, 3)
       c += n;
     }
     if (ok) {
+      // the rows: the final bf16 output (direct) or the fp32 partial
+      // (o * v_scale, max, sum) into split slot jb.slot
       st.finish_sums();
-      write_rows<D, FP8>(p, st, req, qtok, hq, live, direct, slot, tig);
+      st.for_each_run(grp, tig, [&](int row, int d0, float4 v, float, float l) {
+        int r, qt, hq;
+        if (!jb.rows.get(p.g, row, r, qt, hq)) return;
+        if (jb.direct) {
+          const float f = p.v_scale / l;
+          const __nv_bfloat162 a = __floats2bfloat162_rn(v.x * f, v.y * f);
+          const __nv_bfloat162 b = __floats2bfloat162_rn(v.z * f, v.w * f);
+          *reinterpret_cast<uint2*>(p.out + ((int64_t)qt * p.Hq + hq) * D + d0) =
+              make_uint2(*reinterpret_cast<const uint32_t*>(&a),
+                         *reinterpret_cast<const uint32_t*>(&b));
+        } else {
+          const int64_t orow = ((int64_t)r * p.Hq + hq) * p.ws_splits + jb.slot;
+          const float s = p.v_scale;
+          *reinterpret_cast<float4*>(p.ws_o + orow * D + d0) =
+              make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
+        }
+      });
+      if (!jb.direct)
+        st.for_each_stat(grp, tig, [&](int row, float m, float l) {
+          int r, qt, hq;
+          if (jb.rows.get(p.g, row, r, qt, hq))
+            p.ws_ml[((int64_t)r * p.Hq + hq) * p.ws_splits + jb.slot] = make_float2(m, l);
+        });
     }
   }
   // copies still in flight after a wait gave up land before the CTA exits
-  if (!prefix) {
+  if (!jb.prefix) {
     if (!ok && lane == 0)
       for (int c = consumed; c < issued_w; ++c)
         mbar_wait(&cs->full[stage0 + c % sw], (c / sw) & 1, p.err);
@@ -371,6 +294,116 @@ __global__ void __launch_bounds__(kCThreads, 3)
     const int n = cs->issued;
     for (int c = n - S > 0 ? n - S : 0; c < n; ++c) mbar_wait(&cs->full[c % S], (c / S) & 1, p.err);
   }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kCThreads, 3)
+    cascade_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                          const __grid_constant__ CUtensorMap tmap_v, DecodeParams p,
+                          CascadePlan cp) {
+  using G = Geo<D, FP8>;
+  using CG = CascadeGeo<D, FP8>;
+  constexpr int S = CG::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  if constexpr (CG::kSw) ring += (1024u - (smem_u32(smem) & 1023u)) & 1023u;  // 1024-byte aligned
+  CascadeSmem* cs = reinterpret_cast<CascadeSmem*>(ring + S * G::kStageBytes);
+  const int warp = threadIdx.x >> 5;
+
+  // ---- this warp's key run, rows and destination
+  WarpJob jb{};
+  jb.prefix = (int)blockIdx.x < cp.n_prefix_ctas;
+  jb.rows.prefix = jb.prefix;
+  if (jb.prefix) {
+    int b = blockIdx.x;
+    const int rb = b % cp.row_blocks;
+    b /= cp.row_blocks;
+    jb.kvh = b % p.Hkv;
+    b /= p.Hkv;
+    const int piece = b % cp.pieces;
+    const int k = b / cp.pieces;
+    if (k >= p.groups.n) return;
+    const int first = p.groups.first[k], n = p.groups.size[k];
+    const int q_begin = p.qsl[first];
+    if (p.qsl[first + n] - q_begin != n || q_begin < 0 || q_begin + n > p.T) {
+      // members are not all decodes, or a device qsl leaves q / out
+      if (threadIdx.x == 0 && rb == 0 && jb.kvh == 0 && piece == 0)
+        raise_error(p.err, kErrBounds);
+      return;
+    }
+    jb.k_begin = piece * p.groups.prefix_split_tokens;
+    if (jb.k_begin >= p.groups.prefix_tokens[k]) return;
+    jb.k_end = min(p.groups.prefix_tokens[k], jb.k_begin + p.groups.prefix_split_tokens);
+    const int rows = n * p.g;  // (member, head) rows of the group
+    const int row0 = rb * kRowsPerCta;
+    if (row0 >= rows) return;
+    jb.nact = min(kCWarps, (rows - row0 + 15) / 16);
+    jb.table = p.block_tables + (int64_t)first * p.max_blocks;
+    jb.sw = S;
+    jb.stage0 = 0;
+    jb.slot = piece;
+    jb.fills = warp == 0;
+    jb.rows.r0 = row0 + warp * 16;
+    jb.rows.nrows = warp < jb.nact ? min(16, rows - jb.rows.r0) : 0;
+    jb.rows.first = first;
+    jb.rows.q_begin = q_begin;
+    jb.rows.kvh = jb.kvh;
+    // a warp without rows only takes part in the barriers
+    jb.nch = jb.rows.nrows > 0 ? (jb.k_end - jb.k_begin + kChunk - 1) / kChunk : 0;
+    cascade_warp<D, FP8, MmaRows<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
+    return;
+  }
+  const int b = (int)blockIdx.x - cp.n_prefix_ctas;
+  const int r = b / cp.tail_ctas, x = b % cp.tail_ctas;
+  if (r >= p.R) return;
+  const int qs = p.qsl[r];
+  if (p.qsl[r + 1] - qs != 1) return;  // not a decode request
+  const int seq = p.seq_lens[r];
+  if (qs < 0 || qs >= p.T || seq < 1 || seq > p.max_blocks * p.B) {
+    if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int grp_id = group_of(p.groups, r);
+  const int k_lo = grp_id >= 0 ? p.groups.prefix_tokens[grp_id] : 0;
+  const int slot0 = prefix_slots(p.groups, grp_id);
+  if (k_lo >= seq) {
+    if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  const int nsplit = (seq - k_lo + p.split_tokens - 1) / p.split_tokens;
+  const int units = p.Hkv * p.head_groups;  // (kv head, 16-head part) of a split
+  if ((int64_t)nsplit * units > (int64_t)cp.tail_ctas * kCWarps ||
+      (slot0 + nsplit > 1 && slot0 + nsplit > p.ws_splits)) {
+    // device seq_lens disagree with the host mirror the grid was planned from
+    if (threadIdx.x == 0 && x == 0) raise_error(p.err, kErrBounds);
+    return;
+  }
+  if (x * kCWarps >= nsplit * units) return;
+  const int t = x * kCWarps + warp;
+  const int split = t / units, u = t % units;
+  jb.kvh = u / p.head_groups;
+  const int part = u % p.head_groups;
+  jb.rows.nrows = t < nsplit * units ? min(16, p.g - 16 * part) : 0;
+  jb.rows.req = r;
+  jb.rows.qtok = qs;
+  jb.rows.hq0 = jb.kvh * p.g + 16 * part;
+  jb.k_begin = k_lo + split * p.split_tokens;
+  jb.k_end = min(seq, jb.k_begin + p.split_tokens);
+  jb.nch = jb.rows.nrows > 0 ? (jb.k_end - jb.k_begin + kChunk - 1) / kChunk : 0;
+  jb.table = p.block_tables + (int64_t)r * p.max_blocks;
+  jb.nact = 1;
+  jb.sw = CG::kTailStages;
+  jb.stage0 = warp * CG::kTailStages;
+  jb.direct = slot0 + nsplit == 1;
+  jb.slot = slot0 + split;
+  jb.fills = jb.nch > 0;
+  if constexpr (FP8) {  // (as the decode kernels: E4M3 pools, up to 8 heads)
+    if (p.g <= 8) {
+      cascade_warp<D, FP8, MmaKeys<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
+      return;
+    }
+  }
+  cascade_warp<D, FP8, MmaRows<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
 }
 
 template <int D, bool FP8>

@@ -456,12 +456,13 @@ __device__ __forceinline__ void combine_rows(const DecodeParams& p, const float*
   }
 }
 
-template <int D, bool FP8>
+// MR: the warp's MMA state, MmaRows (up to 16 query heads as the MMA rows)
+// or MmaKeys (up to 8 heads as the columns, the keys as the rows).
+template <int D, bool FP8, class MR>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
   using G = Geo<D, FP8>;
-  using MR = MmaRows<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
   extern __shared__ __align__(128) uint8_t smem[];
@@ -618,12 +619,11 @@ struct PersistBars {
   SmemTail t;
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, class MR>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_persist_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
   using G = Geo<D, FP8>;
-  using MR = MmaRows<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int kRows = 16;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -917,7 +917,11 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cu
   CUtensorMap tk, tv;
   cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
   if (e != cudaSuccess) return e;
-  auto k = decode_mma_kernel<D, FP8>;
+  // E4M3 pools, up to 8 heads: the keys as the MMA rows (half the MMAs of
+  // 16 padded rows); bf16 pools keep MmaRows, whose K loads conflict less in
+  // the linear bf16 stages
+  auto k = FP8 && p.g <= 8 ? decode_mma_kernel<D, FP8, MmaKeys<D, FP8>>
+                           : decode_mma_kernel<D, FP8, MmaRows<D, FP8>>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(max_splits, p.Hkv * p.head_groups, R);
@@ -938,7 +942,8 @@ cudaError_t launch_decode_persist_t(const DecodeParams& p, int n_cta, cudaStream
   CUtensorMap tk, tv;
   cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
   if (e != cudaSuccess) return e;
-  auto k = decode_persist_kernel<D, FP8>;
+  auto k = FP8 && p.g <= 8 ? decode_persist_kernel<D, FP8, MmaKeys<D, FP8>>
+                           : decode_persist_kernel<D, FP8, MmaRows<D, FP8>>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   k<<<n_cta, kThreads, smem, s>>>(tk, tv, p);

@@ -358,6 +358,330 @@ struct MmaRows {
       }
     }
   }
+
+  // After finish_sums: the unnormalised output this lane holds, as runs of
+  // four consecutive dims, f(row, first dim, values, row max, row sum) for
+  // rows grp and grp + 8; and each row's (max, sum) once, from one lane:
+  // g(row, m, l).
+  template <class F>
+  __device__ __forceinline__ void for_each_run(int grp, int tig, F&& f) const {
+#pragma unroll
+    for (int ri = 0; ri < 2; ++ri)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int i = 0; i < DG / 4; ++i)
+          f(grp + 8 * ri, DG * (2 * tig + e) + 4 * i,
+            make_float4(o[4 * i][2 * ri + e], o[4 * i + 1][2 * ri + e], o[4 * i + 2][2 * ri + e],
+                        o[4 * i + 3][2 * ri + e]),
+            m[ri], l[ri]);
+  }
+  template <class F>
+  __device__ __forceinline__ void for_each_stat(int grp, int tig, F&& f) const {
+    if (tig == 0) {
+      f(grp, m[0], l[0]);
+      f(grp + 8, m[1], l[1]);
+    }
+  }
+};
+
+// ---------------------------------------------------------------------------
+// The same warp-level decode with the roles of the MMA operands swapped, for
+// GQA groups of at most 8 heads: the 16 keys of a chunk are the MMA rows and
+// the heads the 8 columns,
+//   S^T = K Q^T   (m16n8k16: A = K, 16 keys x 16 dims per k-step; B = Q^T),
+//   O^T += V^T P^T (m16n8k16: A = V^T, 16 dims x 16 keys; B = P^T).
+// A chunk then takes D/16 + D/16 MMAs instead of MmaRows' 2 D/16 + 2 D/16
+// (whose 16 rows are mostly padding for g <= 8), and a lane holds four
+// scores of a chunk instead of eight.
+//  - S: a fixed permutation of the head dimension, the same for Q and K,
+//    gives lane tig the contiguous dims 32 tig .. 32 tig + 31 over the eight
+//    k-steps (D = 128; 16 tig .. for D = 64): k-step j takes dims 4 j + {0,1}
+//    as its k-columns 2 tig, 2 tig + 1 and 4 j + {2,3} as 2 tig + 8, + 9. The
+//    K fragments are then 16-byte loads of key rows grp and grp + 8 (E4M3 at
+//    D = 128: the 16-byte chunks 2 tig, 2 tig + 1 of the 128-byte-swizzled
+//    rows), and Q^T's fragments are head grp's dims, loaded once.
+//  - softmax per head (column): lane (grp, tig) holds the scores of keys grp,
+//    grp + 8 for heads 2 tig, 2 tig + 1; maxima reduce over the eight grp
+//    lanes by xor-shuffles, sums stay per lane until finish_sums.
+//  - P^T: the 16-bit P of keys 0..7 (and 8..15) is transposed in registers by
+//    movmatrix.trans, which turns the accumulator layout (row key, columns
+//    heads) into the B-operand layout (rows keys 2 tig, 2 tig + 1, column
+//    head grp).
+//  - O^T: m-tile mt holds output dims DG grp + 2 mt (row grp) and
+//    DG grp + 2 mt + 1 (row grp + 8), DG = D / 8, so the A fragments come from
+//    the same V rows 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 over dims
+//    DG grp .. DG grp + DG - 1 that MmaRows reads, paired by prmt, and a lane
+//    ends up holding DG contiguous output dims of heads 2 tig, 2 tig + 1.
+// Same numerics as MmaRows: fp32 scores and accumulators, P rounded to 16
+// bits, E4M3 codes widened exactly to f16, queries of E4M3 pools pre-scaled
+// by a power of two per head.
+template <int D, bool FP8>
+struct MmaKeys {
+  static constexpr int KS = D / 16;  // k-steps of S
+  static constexpr int DG = D / 8;   // output dims per lane group
+  static constexpr int MT = DG / 2;  // m-tiles of O^T
+  static constexpr bool kSw = FP8 && D == 128;
+  static constexpr int kLaneDims = D / 4;  // dims of Q and K per lane (tig)
+  using G = Geo<D, FP8>;
+  uint32_t qb[KS][2];  // B fragments of Q^T (head grp): k-step j, dims 4j + {0,1} / {2,3}
+  float sc[2];         // score scale of heads 2 tig, 2 tig + 1 (log2 units)
+  float o[MT][4];      // O^T: [mt] = (dim d0, head 2tig), (d0, 2tig+1), (d0+1, 2tig), (d0+1, 2tig+1)
+  float m[2], l[2];    // heads 2 tig, 2 tig + 1 (l: this lane's keys until finish_sums)
+
+  // Head grp's dims 32 tig .. (D = 128) as raw bf16 words.
+  struct QRaw {
+    uint4 v[kLaneDims / 8];
+  };
+  // rows[0]: the row of head grp (nullptr: a zero padding head); rows[1] is
+  // not used (heads grp + 8 do not exist for g <= 8).
+  static __device__ __forceinline__ void fetch_q(const __nv_bfloat16* const (&rows)[2], QRaw& r,
+                                                 int tig) {
+#pragma unroll
+    for (int i = 0; i < kLaneDims / 8; ++i)
+      r.v[i] = rows[0] ? *reinterpret_cast<const uint4*>(rows[0] + kLaneDims * tig + 8 * i)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __device__ __forceinline__ void load_q(const __nv_bfloat16* const (&rows)[2], float q_scale,
+                                         int tig) {
+    QRaw r;
+    fetch_q(rows, r, tig);
+    load_q(r, q_scale, tig);
+  }
+  __device__ __forceinline__ void load_q(const QRaw& r, float q_scale, int tig) {
+    const unsigned full = 0xffffffffu;
+    float qf[kLaneDims];
+#pragma unroll
+    for (int i = 0; i < kLaneDims / 8; ++i) bf16x8_to_f32(r.v[i], qf + 8 * i);
+    float up = 1.f, s_head = q_scale;
+    if (FP8) {  // head grp's largest magnitude into [2^14, 2^15) before f16 rounding
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < kLaneDims; ++i) amax = fmaxf(amax, fabsf(qf[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(full, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(full, amax, 2));
+      int e2 = 0;
+      if (amax > 0.f) {
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+        e2 = min(100, max(-120, 14 - ex));
+      }
+      up = __uint_as_float((uint32_t)(e2 + 127) << 23);
+      s_head *= __uint_as_float((uint32_t)(127 - e2) << 23);
+    }
+#pragma unroll
+    for (int j = 0; j < KS; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float a = qf[4 * j + 2 * h] * up, b = qf[4 * j + 2 * h + 1] * up;
+        if (FP8) {
+          __half2 x = __floats2half2_rn(a, b);
+          qb[j][h] = *reinterpret_cast<uint32_t*>(&x);
+        } else {
+          __nv_bfloat162 x = __floats2bfloat162_rn(a, b);
+          qb[j][h] = *reinterpret_cast<uint32_t*>(&x);
+        }
+      }
+    // the scales of the two heads this lane's score columns belong to
+    const int lane = threadIdx.x & 31;
+    sc[0] = __shfl_sync(full, s_head, (2 * (lane & 3)) * 4);
+    sc[1] = __shfl_sync(full, s_head, (2 * (lane & 3) + 1) * 4);
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    m[0] = m[1] = -INFINITY;
+    l[0] = l[1] = 0.f;
+  }
+
+  // The K fragments of k-steps 2q, 2q + 1 of key row `row` (lane tig's dims
+  // 8 q .. 8 q + 7 of its run): w[0], w[1] = k-step 2q's (a0|a1, a2|a3 half),
+  // w[2], w[3] = k-step 2q + 1's.
+  static __device__ __forceinline__ void k_words(const uint8_t* krow, int row, int q, int tig,
+                                                 uint32_t (&w)[4]) {
+    if constexpr (FP8) {
+      // 8 codes: dims kLaneDims tig + 8 q .. + 7, in a 16-byte chunk with the
+      // next 8 (swizzled rows at D = 128)
+      const int byte = kLaneDims * tig + 8 * q;
+      const int chunk = byte >> 4;
+      const uint8_t* src =
+          krow + ((kSw ? (chunk ^ (row & 7)) : chunk) << 4) + (byte & 15);
+      const uint2 x = *reinterpret_cast<const uint2*>(src);
+      MmaRows<D, FP8>::widen8(x.x, x.y, w);
+    } else {
+      const uint4 x =
+          *reinterpret_cast<const uint4*>(krow + (kLaneDims * tig + 8 * q) * G::kElt);
+      w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    }
+  }
+
+  static __device__ __forceinline__ void movtrans(uint32_t& x) {
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %0;" : "+r"(x));
+  }
+
+  template <int NC>
+  __device__ __forceinline__ void chunks(const uint8_t* const (&Ks)[NC],
+                                         const uint8_t* const (&Vs)[NC], int key0, int k_end,
+                                         int grp, int tig) {
+    const unsigned full = 0xffffffffu;
+    // S^T of chunk c: two accumulator chains (even / odd k-step pairs)
+    float s[NC][4];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      float acc[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) acc[h][0] = acc[h][1] = acc[h][2] = acc[h][3] = 0.f;
+      const uint8_t* r0 = Ks[c] + grp * G::kRowBytes;
+      const uint8_t* r1 = Ks[c] + (grp + 8) * G::kRowBytes;
+#pragma unroll
+      for (int q = 0; q < KS / 2; ++q) {
+        uint32_t w0[4], w1[4];
+        k_words(r0, grp, q, tig, w0);
+        k_words(r1, grp + 8, q, tig, w1);
+        MmaRows<D, FP8>::mma(acc[q & 1], w0[0], w1[0], w0[1], w1[1], qb[2 * q][0], qb[2 * q][1]);
+        MmaRows<D, FP8>::mma(acc[q & 1], w0[2], w1[2], w0[3], w1[3], qb[2 * q + 1][0],
+                             qb[2 * q + 1][1]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) s[c][i] = acc[0][i] + acc[1][i];
+    }
+    // scale, mask, online softmax of heads 2 tig (c0, c2) and 2 tig + 1 (c1, c3)
+    float alpha[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float& x = s[c][2 * h + e];
+          x = key0 + 16 * c + grp + 8 * h < k_end ? x * sc[e] : -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
+      const float m_new = fmaxf(m[e], mx);
+      alpha[e] = ex2_ftz(m[e] - m_new);
+      float ps = 0.f;
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float& x = s[c][2 * h + e];
+          x = ex2_ftz(x - m_new);
+          ps += x;
+        }
+      l[e] = l[e] * alpha[e] + ps;
+      m[e] = m_new;
+    }
+    if (__any_sync(full, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+    }
+    auto pk = [](float x, float y) -> uint32_t {
+      if (FP8) {
+        __half2 h = __floats2half2_rn(x, y);
+        return *reinterpret_cast<uint32_t*>(&h);
+      }
+      __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+      return *reinterpret_cast<uint32_t*>(&h);
+    };
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      // P^T of chunk c as the B fragments: keys 2 tig, 2 tig + 1 (and + 8) of head grp
+      uint32_t b0 = pk(s[c][0], s[c][1]), b1 = pk(s[c][2], s[c][3]);
+      movtrans(b0);
+      movtrans(b1);
+      // V rows 2tig, 2tig+1, 2tig+8, 2tig+9 over dims DG grp .. DG grp + DG - 1
+      uint32_t vw[4][DG / 2];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int kr = 2 * tig + (i & 1) + 8 * (i >> 1);
+        if constexpr (kSw) {  // the 16-byte chunk grp of row kr, stored at grp ^ (kr & 7)
+          const uint4 x = *reinterpret_cast<const uint4*>(Vs[c] + kr * G::kRowBytes +
+                                                          ((grp ^ (kr & 7)) << 4));
+          MmaRows<D, FP8>::widen8(x.x, x.y, &vw[i][0]);
+          MmaRows<D, FP8>::widen8(x.z, x.w, &vw[i][4]);
+        } else {
+          const uint8_t* vrow = Vs[c] + kr * G::kRowBytes + DG * grp * G::kElt;
+#pragma unroll
+          for (int h = 0; h < DG / 8; ++h) {
+            uint32_t w4[4];
+            MmaRows<D, FP8>::load8(vrow + 8 * h * G::kElt, w4);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
+          }
+        }
+        if (key0 + 16 * c + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
+#pragma unroll
+          for (int w = 0; w < DG / 2; ++w) vw[i][w] = 0u;
+      }
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a0) : "r"(vw[0][mt]), "r"(vw[1][mt]));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a1) : "r"(vw[0][mt]), "r"(vw[1][mt]));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a2) : "r"(vw[2][mt]), "r"(vw[3][mt]));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(a3) : "r"(vw[2][mt]), "r"(vw[3][mt]));
+        MmaRows<D, FP8>::mma(o[mt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void chunk(const uint8_t* Ks, const uint8_t* Vs, int key0, int k_end,
+                                        int grp, int tig) {
+    const uint8_t* const k[1] = {Ks};
+    const uint8_t* const v[1] = {Vs};
+    chunks<1>(k, v, key0, k_end, grp, tig);
+  }
+
+  // Per-head sums over the eight key lanes of a head (the maxima already agree).
+  __device__ __forceinline__ void finish_sums() {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 4);
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 8);
+      l[e] += __shfl_xor_sync(0xffffffffu, l[e], 16);
+    }
+  }
+
+  template <class F>
+  __device__ __forceinline__ void for_each_run(int grp, int tig, F&& f) const {
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int i = 0; i < DG / 4; ++i)
+        f(2 * tig + e, DG * grp + 4 * i,
+          make_float4(o[2 * i][e], o[2 * i][2 + e], o[2 * i + 1][e], o[2 * i + 1][2 + e]), m[e],
+          l[e]);
+  }
+  template <class F>
+  __device__ __forceinline__ void for_each_stat(int grp, int tig, F&& f) const {
+    if (grp == 0) {
+      f(2 * tig, m[0], l[0]);
+      f(2 * tig + 1, m[1], l[1]);
+    }
+  }
+
+  // This warp's rows (heads < nrows) into the combine buffer of warp `warp`.
+  __device__ __forceinline__ void to_comb(float* comb_o, float* comb_m, float* comb_l, int warp,
+                                          int nrows, int grp, int tig) const {
+    for_each_run(grp, tig, [&](int row, int d0, float4 v, float, float) {
+      if (row < nrows) *reinterpret_cast<float4*>(comb_o + (warp * 16 + row) * D + d0) = v;
+    });
+    for_each_stat(grp, tig, [&](int row, float mm, float ll) {
+      if (row < nrows) {
+        comb_m[warp * 16 + row] = mm;
+        comb_l[warp * 16 + row] = ll;
+      }
+    });
+  }
 };
 
 // TMA maps of the E4M3 pools at D = 128 (the swizzled stages): a pool as
