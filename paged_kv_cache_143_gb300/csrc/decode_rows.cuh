@@ -189,6 +189,18 @@ struct MmaRows {
     }
   }
 
+  // The reference maximum of a row after a step whose largest score is mx
+  // (log2 units): it moves to the new maximum only when that exceeds the
+  // current reference by more than 2^8 (alpha = the factor that rescales
+  // what was accumulated against the old reference; 1 when it stays). A stale
+  // reference is exact algebra (every accumulated term and the sum share
+  // it); it bounds the step's weights P by 2^8 and skips most rescales.
+  static __device__ __forceinline__ float rebase(float m_cur, float mx, float& alpha) {
+    const bool move = mx > m_cur + 8.f;  // (also the first step: m_cur = -inf)
+    alpha = move ? ex2_ftz(m_cur - mx) : 1.f;
+    return move ? mx : m_cur;
+  }
+
   // NC consecutive 16-key chunks (K rows Ks[c], V rows Vs[c], keys key0 +
   // 16 c .. key0 + 16 c + 15, those at or past k_end masked): scores, one
   // online-softmax update over all NC * 16 keys, O += P V. Two chunks per call
@@ -236,6 +248,7 @@ struct MmaRows {
       }
     }
     // scale, mask, online softmax of rows grp (c0, c1) and grp + 8 (c2, c3)
+    const bool whole = key0 + 16 * NC <= k_end;  // no key of the step is masked
     float alpha[2];
 #pragma unroll
     for (int ri = 0; ri < 2; ++ri) {
@@ -245,24 +258,23 @@ struct MmaRows {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float& x = s[t][2 * ri + e];
-          x = key0 + 8 * t + 2 * tig + e < k_end ? x * sc[ri] : -INFINITY;
+          x = whole || key0 + 8 * t + 2 * tig + e < k_end ? x * sc[ri] : -INFINITY;
           mx = fmaxf(mx, x);
         }
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
-      const float m_new = fmaxf(m[ri], mx);
-      alpha[ri] = ex2_ftz(m[ri] - m_new);
+      const float m_ref = rebase(m[ri], mx, alpha[ri]);
       float ps = 0.f;
 #pragma unroll
       for (int t = 0; t < NT; ++t)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           float& x = s[t][2 * ri + e];
-          x = ex2_ftz(x - m_new);
+          x = ex2_ftz(x - m_ref);
           ps += x;
         }
       l[ri] = l[ri] * alpha[ri] + ps;
-      m[ri] = m_new;
+      m[ri] = m_ref;
     }
     if (__any_sync(full, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
@@ -307,7 +319,7 @@ struct MmaRows {
             for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
           }
         }
-        if (key0 + 16 * c + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
+        if (!whole && key0 + 16 * c + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
 #pragma unroll
           for (int w = 0; w < DG / 2; ++w) vw[i][w] = 0u;
       }
@@ -546,6 +558,7 @@ struct MmaKeys {
       for (int i = 0; i < 4; ++i) s[c][i] = acc[0][i] + acc[1][i];
     }
     // scale, mask, online softmax of heads 2 tig (c0, c2) and 2 tig + 1 (c1, c3)
+    const bool whole = key0 + 16 * NC <= k_end;  // no key of the step is masked
     float alpha[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
@@ -555,25 +568,24 @@ struct MmaKeys {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float& x = s[c][2 * h + e];
-          x = key0 + 16 * c + grp + 8 * h < k_end ? x * sc[e] : -INFINITY;
+          x = whole || key0 + 16 * c + grp + 8 * h < k_end ? x * sc[e] : -INFINITY;
           mx = fmaxf(mx, x);
         }
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(full, mx, 16));
-      const float m_new = fmaxf(m[e], mx);
-      alpha[e] = ex2_ftz(m[e] - m_new);
+      const float m_ref = MmaRows<D, FP8>::rebase(m[e], mx, alpha[e]);
       float ps = 0.f;
 #pragma unroll
       for (int c = 0; c < NC; ++c)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           float& x = s[c][2 * h + e];
-          x = ex2_ftz(x - m_new);
+          x = ex2_ftz(x - m_ref);
           ps += x;
         }
       l[e] = l[e] * alpha[e] + ps;
-      m[e] = m_new;
+      m[e] = m_ref;
     }
     if (__any_sync(full, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
@@ -618,7 +630,7 @@ struct MmaKeys {
             for (int w = 0; w < 4; ++w) vw[i][4 * h + w] = w4[w];
           }
         }
-        if (key0 + 16 * c + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
+        if (!whole && key0 + 16 * c + kr >= k_end)  // unwritten cells may hold NaN; P = 0 must not meet them
 #pragma unroll
           for (int w = 0; w < DG / 2; ++w) vw[i][w] = 0u;
       }
