@@ -301,6 +301,7 @@ __global__ void __launch_bounds__(kCThreads, 3)
     cascade_decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DecodeParams p,
                           CascadePlan cp) {
+  launch_dependents();  // the merge that follows may be scheduled now
   using G = Geo<D, FP8>;
   using CG = CascadeGeo<D, FP8>;
   constexpr int S = CG::kStages;

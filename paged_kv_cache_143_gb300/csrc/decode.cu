@@ -169,6 +169,7 @@ __device__ __forceinline__ void produce(const DecodeParams& p, uint8_t* ring, Sm
 // GH heads per warp, HG head groups per CTA (GH * HG = g).
 template <int D, bool FP8, int GH, int HG>
 __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeParams p) {
+  launch_dependents();  // the merge that follows may be scheduled now
   using G = Geo<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int CR = kConsumerWarps / HG;  // warps per head group (chunk residues)
@@ -462,6 +463,7 @@ template <int D, bool FP8, class MR>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
+  launch_dependents();  // the merge that follows may be scheduled now
   using G = Geo<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int kRows = 16;        // MMA rows (query heads, zero padded)
@@ -623,6 +625,7 @@ template <int D, bool FP8, class MR>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_persist_kernel(const __grid_constant__ CUtensorMap tmap_k,
                           const __grid_constant__ CUtensorMap tmap_v, DecodeParams p) {
+  launch_dependents();  // the merge that follows may be scheduled now
   using G = Geo<D, FP8>;
   constexpr int kStages = G::kStages;
   constexpr int kRows = 16;
@@ -824,6 +827,7 @@ constexpr int kMergeWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(DecodeParams p) {
   constexpr int kV = D / 32;  // dims per lane
+  grid_dependency_wait();  // the decode grid's partials are complete and visible
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.x * kMergeWarps + (threadIdx.x >> 5), r = blockIdx.y;
   if (h >= p.Hq) return;
@@ -986,12 +990,20 @@ cudaError_t launch_decode_persist(const DecodeParams& p, int D, bool fp8, int n_
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int D, int R, cudaStream_t s) {
-  dim3 grid((p.Hq + kMergeWarps - 1) / kMergeWarps, R);
-  if (D == 128)
-    merge_kernel<128><<<grid, kMergeWarps * 32, 0, s>>>(p);
-  else
-    merge_kernel<64><<<grid, kMergeWarps * 32, 0, s>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent launch: scheduled while the decode grid before
+  // it drains, it waits for that grid's partials in grid_dependency_wait
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((p.Hq + kMergeWarps - 1) / kMergeWarps, R);
+  cfg.blockDim = dim3(kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return D == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<128>, p)
+                  : cudaLaunchKernelEx(&cfg, merge_kernel<64>, p);
 }
 
 }  // namespace pa

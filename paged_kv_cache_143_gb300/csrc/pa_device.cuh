@@ -96,6 +96,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsign
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel that produces split partials lets the merge kernel that follows
+// it on the stream be scheduled early (launch_dependents, called by every
+// CTA at its start); the merge waits (grid_dependency_wait) until the
+// producing grid has completed and its writes are visible. Both are no-ops
+// for kernels launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------- bulk async copies
 
 // One contiguous global -> shared copy completed on `bar` (transaction bytes).
