@@ -183,8 +183,8 @@ pa_status pa_forward(const void* q, void* out, const int32_t* query_start_loc,
  * exact arithmetic; the fp32 summation order differs): the softmax over the
  * union of the prefix keys and the tail keys is taken in parts, the prefix
  * pieces and the tail splits, merged by log-sum-exp. Each group's prefix K/V
- * is read once for all of its members (a tensor-core tile whose rows are the
- * members' decode tokens x the GQA heads) instead of once per member.
+ * is read once for every 64 of its (member, GQA head) rows (four warps share
+ * each staged K/V chunk) instead of once per member; any GQA width.
  *
  * Arguments as pa_forward, plus:
  *   num_groups          G, 0 <= G <= 64 (more: PA_ERR_UNSUPPORTED). G == 0

@@ -1,8 +1,8 @@
 """GPU parity of pa_forward_shared_prefix (each group's shared prefix read once
-by a tensor-core tile over all members' decode tokens, private tails by the
-decode kernels, parts merged by log-sum-exp) against the fp64 oracle, which
-knows nothing of groups: it gathers every request's blocks through its own
-table row."""
+for every 64 of its (member, head) rows by warps sharing a ring of K/V
+stages, private tails by one warp per task, parts merged by log-sum-exp)
+against the fp64 oracle, which knows nothing of groups: it gathers every
+request's blocks through its own table row."""
 import numpy as np
 import pytest
 import torch
@@ -55,6 +55,12 @@ CASES = [
      [("g", 16, [1]), ("g", 32, [3, 4]), ("d", 5), ("g", 1024, [700, 1, 2])]),
     ("g4_fp8_mixed", 32, 8, 128, 16, "fp8",
      [("p", 900, 300), ("g", 512, [7, 100, 513, 1] * 3), ("d", 1500), ("g", 2048, [9] * 17)]),
+    # 40 members x 4 heads = 160 rows: three 64-row blocks per prefix piece;
+    # a 1040-key prefix: pieces of 512, 512 and 16 keys
+    ("g4_fp8_wide_groups", 32, 8, 128, 16, "fp8",
+     [("g", 256, [3, 40, 1, 77] * 10), ("g", 1040, [1, 2, 700]), ("d", 33)]),
+    ("g8_fp8_b32", 16, 2, 128, 32, "fp8",
+     [("g", 3072, [1, 31, 32, 33, 600]), ("d", 4000)]),
 ]
 
 
