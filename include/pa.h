@@ -379,6 +379,23 @@ pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src, const int32
                          int32_t n, pa_stream_t stream);
 
 /*
+ * pa_gather_rows — dst row i = src row rows[i], for i < n: the rows a step
+ * hands on (each request's last query token, whose output the sampler
+ * needs) gathered by index, as [MRV2, "재설계 1"] gathers the persistent
+ * batch's rows by idx_mapping.
+ *
+ *   src        dev, src_rows rows of row_bytes bytes (16-byte aligned)
+ *   row_bytes  a positive multiple of 16
+ *   rows       dev int32 [n]
+ *   dst        dev, n rows of row_bytes bytes (16-byte aligned), not
+ *              overlapping src
+ * A row index outside [0, src_rows) sets PA_ERR_DEVICE_BOUNDS and that dst
+ * row is left unchanged. n == 0 is a no-op. Argument errors: PA_ERR_INVALID.
+ */
+pa_status pa_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes,
+                         const int32_t* rows, int32_t n, void* dst, pa_stream_t stream);
+
+/*
  * pa_get_error — synchronise `stream`, then return and clear the sticky
  * device error word of the current device: PA_ERR_TIMEOUT if a bounded wait
  * gave up, else PA_ERR_DEVICE_BOUNDS if an index was out of range, else

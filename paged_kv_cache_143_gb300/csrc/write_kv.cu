@@ -1,12 +1,13 @@
 // write_kv.cu — pa_write_kv (scatter new K/V by slot_mapping, bf16 copy or
-// FP8 E4M3 store) and pa_copy_blocks (whole-block copy for copy-on-write).
+// FP8 E4M3 store), pa_copy_blocks (whole-block copy for copy-on-write) and
+// pa_gather_rows (rows of a device array gathered by index).
 //
 // [vLLM-wiki "블록 테이블"]: token t goes to slot s = block * B + offset.
 // [vLLM-wiki "엔진 구조와 주요 기능"], [V1-blog "FP8 KV 캐시 양자화의 네이티브 통합"]:
 // the cache may be stored as 8-bit floats with a per-tensor scale.
 // [vLLM-wiki "블록 공유와 쓰기 시 복사"]: a shared block is copied before a write.
 //
-// Both kernels are HBM scatter/copy work: every thread moves one 16-byte
+// The kernels are HBM scatter/copy/gather work: every thread moves one 16-byte
 // vector; consecutive threads cover consecutive bytes of one (token, head) row
 // so loads and stores are coalesced.
 #include <cuda_fp8.h>
@@ -139,5 +140,44 @@ extern "C" pa_status pa_copy_blocks(const pa_kv_pool* pool, const int32_t* src,
   copy_blocks_kernel<<<grid, 256, 0, pa::as_stream(stream)>>>(
       static_cast<uint8_t*>(pool->k_pool), static_cast<uint8_t*>(pool->v_pool), src, dst,
       pool->num_blocks, block_bytes, err);
+  return pa::launch_status();
+}
+
+namespace {
+
+// dst row i = src row rows[i]; one thread per 16-byte vector (grid-stride).
+__global__ void gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                   const int32_t* __restrict__ rows, int64_t n_vec,
+                                   int64_t vec_per_row, int64_t src_rows, unsigned* err) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vec;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / vec_per_row, v = i - row * vec_per_row;
+    const int32_t r = __ldg(rows + row);
+    if (r < 0 || r >= src_rows) {
+      if (v == 0) pa::raise_error(err, kErrBounds);
+      continue;
+    }
+    dst[i] = src[(int64_t)r * vec_per_row + v];
+  }
+}
+
+}  // namespace
+
+extern "C" pa_status pa_gather_rows(const void* src, int64_t src_rows, int64_t row_bytes,
+                                    const int32_t* rows, int32_t n, void* dst,
+                                    pa_stream_t stream) {
+  if (n < 0 || src_rows < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return PA_ERR_INVALID;
+  if (n == 0) return PA_OK;
+  if (!src || !dst || !rows || !pa::aligned16(src) || !pa::aligned16(dst)) return PA_ERR_INVALID;
+  unsigned* err = pa::error_word();
+  if (!err) return PA_ERR_CUDA;
+  const int64_t vec_per_row = row_bytes / 16, n_vec = (int64_t)n * vec_per_row;
+  const int threads = 256;
+  int64_t blocks = (n_vec + threads - 1) / threads;
+  const int64_t cap = (int64_t)pa::num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<(unsigned)blocks, threads, 0, pa::as_stream(stream)>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), rows, n_vec, vec_per_row,
+      src_rows, err);
   return pa::launch_status();
 }

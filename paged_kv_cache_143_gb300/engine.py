@@ -11,7 +11,8 @@ copy; then, on the stream,
   pa_prepare_inputs       query_start_loc, seq_lens, positions, slot mapping,
   pa_write_kv             the step's new K/V,
   pa_forward              attention for every entry,
-and the output row of each entry's last token is read back.
+  pa_gather_rows          the output row of each entry's last token,
+and those rows are read back into one of two pinned host buffers.
 
 [MRV2 "재설계 1"] persistent slots and idx_mapping; [MRV2 "재설계 2"] the
 host never modifies a buffer the device may still be reading: two pinned
@@ -58,7 +59,14 @@ class Engine:
         n = pa.forward_workspace_size(max_reqs, num_q_heads, self.D, max_splits)
         self.ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
         self.mirror = np.full(max_reqs, -1, np.int64)  # stored-token count the device holds
-        self.out_host = None
+        # each entry's last output row: gathered on the device, read back into
+        # one of two pinned buffers (a step's rows stay valid through the next step)
+        self.last_dev = torch.empty((max_reqs, num_q_heads, self.D), dtype=torch.bfloat16,
+                                    device=dev)
+        self.last_host = [torch.empty((max_reqs, num_q_heads, self.D),
+                                      dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+        self.last_turn = 0
+        self.last_out = None
         self.turn = 0
         self.steps = 0
         self.h2d_bytes = 0
@@ -69,7 +77,8 @@ class Engine:
         """Runs one step; q/k/v/out hold at least the step's tokens as rows.
         Returns the scheduled batch; the output rows of each entry's last
         token are in `last_out` (host, pinned) once the step's stream has
-        reached the end of the step (the next `step` or `sync` waits)."""
+        reached the end of the step (the next `step` or `sync` waits); they
+        stay valid through the next step (two buffers alternate)."""
         b = self.sched.step()
         R, T = b.num_reqs, b.num_tokens
         if T > self.max_tokens or R > self.max_reqs:
@@ -116,11 +125,15 @@ class Engine:
             pa.forward(q[:T], out[:T], self.qsl[:R + 1], self.seq[:R], b.query_start_loc,
                        b.seq_lens, self.gathered[:R], self.pool, self.scale, 1,
                        workspace=self.ws, stream=s)
-            rows = out.index_select(0, d[12].long()) if R else out[:0]
-            self.last_out = rows.to("cpu", non_blocking=True)
+            host = self.last_host[self.last_turn][:R]
+            if R:
+                pa.gather_rows(out, d[12], self.last_dev[:R], stream=s)
+                host.copy_(self.last_dev[:R], non_blocking=True)
+            self.last_out = host
+            self.last_turn ^= 1
         self.mirror[b.idx_mapping] = b.seq_lens
         self.h2d_bytes += 4 * total
-        self.d2h_bytes += rows.numel() * rows.element_size()
+        self.d2h_bytes += host.numel() * host.element_size()
         self.steps += 1
         self.stream = s
         return b

@@ -23,7 +23,8 @@ PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
 
 # every function declared in include/pa.h
 EXPORTS = ("pa_write_kv", "pa_forward_workspace_size", "pa_forward", "pa_apply_staged_writes",
-           "pa_copy_blocks", "pa_get_error", "pa_status_string", "pa_kernel_launches",
+           "pa_copy_blocks", "pa_gather_rows", "pa_get_error", "pa_status_string",
+           "pa_kernel_launches",
            "pa_forward_noalloc", "pa_selftest_wait_timeout", "pa_forward_shared_prefix",
            "pa_prepare_inputs", "pa_decode_graph_create", "pa_decode_graph_launch",
            "pa_decode_graph_destroy", "pa_decode_graph_kernels",
@@ -113,6 +114,8 @@ def lib():
         L.pa_apply_staged_writes.argtypes = [P, I32, I32, P, P, P, P, I32, P, I32, P, P]
         L.pa_copy_blocks.restype = ctypes.c_int
         L.pa_copy_blocks.argtypes = [PP, P, P, I32, P]
+        L.pa_gather_rows.restype = ctypes.c_int
+        L.pa_gather_rows.argtypes = [P, I64, I64, P, I32, P, P]
         L.pa_get_error.restype = ctypes.c_int
         L.pa_get_error.argtypes = [P]
         L.pa_status_string.restype = ctypes.c_char_p
@@ -543,6 +546,18 @@ def copy_blocks(pool: KVPool, src: torch.Tensor, dst: torch.Tensor, stream=None)
     st = lib().pa_copy_blocks(pool.ref(), _dptr(src, torch.int32),
                               _dptr(dst, torch.int32), src.numel(), _stream(stream))
     _check(st, "pa_copy_blocks")
+
+
+def gather_rows(src: torch.Tensor, rows: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """dst[i] = src[rows[i]] (rows of src's first dimension) on the device."""
+    n = rows.numel()
+    if dst.shape[0] < n or dst.shape[1:] != src.shape[1:] or dst.dtype != src.dtype:
+        raise ValueError("dst must hold len(rows) rows shaped like src's")
+    if not (src.is_contiguous() and dst.is_contiguous()):
+        raise ValueError("src and dst must be contiguous")
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 16
+    _check(lib().pa_gather_rows(_dptr(src), src.shape[0], row_bytes, _dptr(rows, torch.int32), n,
+                                _dptr(dst), _stream(stream)), "pa_gather_rows")
 
 
 def selftest_wait_timeout(stream=None) -> None:

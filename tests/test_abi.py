@@ -207,3 +207,17 @@ def test_prefill_gqa_wider_than_a_tile_is_refused():
     st = L.pa_forward(16, 16, 16, 16, ptr(qsl), ptr(seq), 16, 4, 1, 3, 256,
                       ctypes.byref(pool), 0.125, 1, None, 0, None)
     assert st == pa.PA_ERR_UNSUPPORTED
+
+
+def test_gather_rows_host_rejections():
+    """pa_gather_rows checks its arguments on the host before any launch
+    (fake, aligned device pointers are never touched)."""
+    L = pa.lib()
+    assert L.pa_gather_rows(16, 10, 256, 16, 0, 16, None) == pa.PA_OK  # nothing to gather
+    assert L.pa_gather_rows(16, 10, 256, 16, -1, 16, None) == pa.PA_ERR_INVALID
+    assert L.pa_gather_rows(16, 10, 24, 16, 3, 16, None) == pa.PA_ERR_INVALID  # not 16-byte rows
+    assert L.pa_gather_rows(16, 10, 0, 16, 3, 16, None) == pa.PA_ERR_INVALID
+    assert L.pa_gather_rows(None, 10, 256, 16, 3, 16, None) == pa.PA_ERR_INVALID
+    assert L.pa_gather_rows(16, 10, 256, None, 3, 16, None) == pa.PA_ERR_INVALID
+    assert L.pa_gather_rows(24, 10, 256, 16, 3, 16, None) == pa.PA_ERR_INVALID  # misaligned src
+    assert L.pa_gather_rows(16, -1, 256, 16, 3, 16, None) == pa.PA_ERR_INVALID

@@ -224,3 +224,25 @@ def test_copy_blocks_bit_exact(cuda_device, dtype):
     gk, gv = pool_bits(pool)
     np.testing.assert_array_equal(gk, ref.k)
     np.testing.assert_array_equal(gv, ref.v)
+
+
+def test_gather_rows_bit_exact_and_flags_bad_rows(cuda_device):
+    """pa_gather_rows: dst[i] = src[rows[i]] bit for bit (repeated and
+    unordered rows), against a numpy gather of the same bytes; a row index
+    outside src sets PA_ERR_DEVICE_BOUNDS and leaves that dst row as it was."""
+    g = torch.Generator().manual_seed(31)
+    src = torch.randn((300, 32, 128), generator=g).bfloat16()
+    rows = torch.tensor([5, 299, 0, 5, 17, 123, 298, 1], dtype=torch.int32)
+    dst = torch.full((8, 32, 128), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    pa.gather_rows(src.to(cuda_device), rows.to(cuda_device), dst)
+    assert pa.get_error() == pa.PA_OK
+    want = src.view(torch.int16).numpy()[rows.numpy()]
+    np.testing.assert_array_equal(dst.cpu().view(torch.int16).numpy(), want)
+    bad = torch.tensor([2, 300, -1, 4], dtype=torch.int32, device=cuda_device)
+    dst2 = torch.full((4, 32, 128), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    pa.gather_rows(src.to(cuda_device), bad, dst2)
+    assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS
+    got = dst2.cpu().view(torch.int16).numpy()
+    np.testing.assert_array_equal(got[0], src.view(torch.int16).numpy()[2])
+    np.testing.assert_array_equal(got[3], src.view(torch.int16).numpy()[4])
+    assert (dst2[1:3].float() == 7.0).all()
