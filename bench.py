@@ -278,6 +278,7 @@ def run_libpa(args):
                      "ms_per_launch": round(fwd_ms, 5),
                      "traffic": traffic_for("decode_kernel", [
                          "paged_kv_cache_143_gb300/csrc/decode.cu",
+                         "paged_kv_cache_143_gb300/csrc/decode_rows.cuh",
                          "paged_kv_cache_143_gb300/csrc/pa_device.cuh"])},
         "e2e": e2e,
         "clocks": clk,
@@ -360,7 +361,8 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
     import workloads
     from paged_kv_cache_143_gb300 import accounting, pa
     stream = torch.cuda.current_stream()
-    w = workloads.make(cfg, device=dev, kv_dtype=kv_dtype)
+    n_req = getattr(args, "long_requests", None) if cfg == 5 else None
+    w = workloads.make(cfg, device=dev, kv_dtype=kv_dtype, num_requests=n_req)
     step = Step(w, dev, max_splits=32)
     ms = timed(step.run, args.steps, args.warmup, stream)
     if pa.get_error() != pa.PA_OK:
@@ -599,7 +601,8 @@ def run_serving(args, dev, steps=30):
             "kv_used_blocks": st["used_blocks"], "preemptions": st["preemptions"] -
             st0["preemptions"],
             "step": "pa_sched_step + one pinned upload + pa_apply_staged_writes x2 + "
-                    "pa_copy_blocks + pa_prepare_inputs + pa_write_kv + pa_forward + read-back"}
+                    "pa_copy_blocks + pa_prepare_inputs + pa_write_kv + pa_forward + "
+                    "pa_gather_rows + read-back"}
 
 
 def load_peaks_tensor():
@@ -803,6 +806,9 @@ def main():
     ap.add_argument("--requests", type=int, default=256,
                     help="decode batch size (256 is the benchmark workload; smaller sizes "
                          "are for profiling captures)")
+    ap.add_argument("--long-requests", type=int, default=None,
+                    help="long-context legs: requests of 32768 tokens (32 is the benchmark "
+                         "workload; fewer are for profiling captures)")
     ap.add_argument("--no-cpu", dest="cpu_legs", action="store_false",
                     help="skip the oracle timings on the host cores (profiling runs)")
     ap.add_argument("--chunks", type=int, default=None,
