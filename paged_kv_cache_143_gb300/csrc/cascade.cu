@@ -14,8 +14,8 @@
 // runs the warp-level tensor-core decode (decode_rows.cuh: mma.sync
 // m16n8k16, S and P.V per 16-key chunk, two chunks per online-softmax
 // update, everything in registers; tails of GQA groups of at most 8 heads
-// of E4M3 pools with the keys as the MMA rows). Nothing is combined across warps: a warp
-// writes its rows' partial (or final) output itself.
+// with the keys as the MMA rows). Nothing is combined across
+// warps: a warp writes its rows' partial (or final) output itself.
 //  - prefix CTA (group k, piece, kv head, row block): rows = (member, head)
 //    pairs of the group, 64 per CTA (16 per warp), against one piece of the
 //    prefix read through the first member's table row. The four warps share
@@ -398,13 +398,10 @@ __global__ void __launch_bounds__(kCThreads, 3)
   jb.direct = slot0 + nsplit == 1;
   jb.slot = slot0 + split;
   jb.fills = jb.nch > 0;
-  if constexpr (FP8) {  // (as the decode kernels: E4M3 pools, up to 8 heads)
-    if (p.g <= 8) {
-      cascade_warp<D, FP8, MmaKeys<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
-      return;
-    }
-  }
-  cascade_warp<D, FP8, MmaRows<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
+  if (p.g <= 8)
+    cascade_warp<D, FP8, MmaKeys<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
+  else
+    cascade_warp<D, FP8, MmaRows<D, FP8>>(&tmap_k, &tmap_v, p, ring, cs, jb);
 }
 
 template <int D, bool FP8>

@@ -921,11 +921,9 @@ cudaError_t launch_decode_mma_t(const DecodeParams& p, int R, int max_splits, cu
   CUtensorMap tk, tv;
   cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
   if (e != cudaSuccess) return e;
-  // E4M3 pools, up to 8 heads: the keys as the MMA rows (half the MMAs of
-  // 16 padded rows); bf16 pools keep MmaRows, whose K loads conflict less in
-  // the linear bf16 stages
-  auto k = FP8 && p.g <= 8 ? decode_mma_kernel<D, FP8, MmaKeys<D, FP8>>
-                           : decode_mma_kernel<D, FP8, MmaRows<D, FP8>>;
+  // up to 8 heads: the keys as the MMA rows (half the MMAs of 16 padded rows)
+  auto k = p.g <= 8 ? decode_mma_kernel<D, FP8, MmaKeys<D, FP8>>
+                    : decode_mma_kernel<D, FP8, MmaRows<D, FP8>>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(max_splits, p.Hkv * p.head_groups, R);
@@ -946,8 +944,8 @@ cudaError_t launch_decode_persist_t(const DecodeParams& p, int n_cta, cudaStream
   CUtensorMap tk, tv;
   cudaError_t e = decode_maps<D, FP8>(p, &tk, &tv);
   if (e != cudaSuccess) return e;
-  auto k = FP8 && p.g <= 8 ? decode_persist_kernel<D, FP8, MmaKeys<D, FP8>>
-                           : decode_persist_kernel<D, FP8, MmaRows<D, FP8>>;
+  auto k = p.g <= 8 ? decode_persist_kernel<D, FP8, MmaKeys<D, FP8>>
+                    : decode_persist_kernel<D, FP8, MmaRows<D, FP8>>;
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   k<<<n_cta, kThreads, smem, s>>>(tk, tv, p);

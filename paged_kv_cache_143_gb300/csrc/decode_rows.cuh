@@ -407,12 +407,15 @@ struct MmaRows {
 // (whose 16 rows are mostly padding for g <= 8), and a lane holds four
 // scores of a chunk instead of eight.
 //  - S: a fixed permutation of the head dimension, the same for Q and K,
-//    gives lane tig the contiguous dims 32 tig .. 32 tig + 31 over the eight
-//    k-steps (D = 128; 16 tig .. for D = 64): k-step j takes dims 4 j + {0,1}
-//    as its k-columns 2 tig, 2 tig + 1 and 4 j + {2,3} as 2 tig + 8, + 9. The
-//    K fragments are then 16-byte loads of key rows grp and grp + 8 (E4M3 at
-//    D = 128: the 16-byte chunks 2 tig, 2 tig + 1 of the 128-byte-swizzled
-//    rows), and Q^T's fragments are head grp's dims, loaded once.
+//    gives lane tig eight dims per pair of k-steps: k-steps 2q and 2q + 1
+//    take dims b + {0,1}, b + {2,3} and b + {4,5}, b + {6,7} as their
+//    k-columns (2 tig, 2 tig + 1) and (2 tig + 8, + 9), where b is
+//    D/4 tig + 8 q for E4M3 pools (a lane's dims are one contiguous run: its
+//    8-byte loads of the 128-byte-swizzled rows, or of the 64-byte rows at
+//    D = 64, fall on distinct banks) and 32 q + 8 tig for bf16 pools (the four
+//    lanes of a row read 64 contiguous bytes per load, as MmaRows does). The
+//    K fragments are then loads of key rows grp and grp + 8, and Q^T's
+//    fragments are head grp's dims, loaded once.
 //  - softmax per head (column): lane (grp, tig) holds the scores of keys grp,
 //    grp + 8 for heads 2 tig, 2 tig + 1; maxima reduce over the eight grp
 //    lanes by xor-shuffles, sums stay per lane until finish_sums.
@@ -441,17 +444,21 @@ struct MmaKeys {
   float o[MT][4];      // O^T: [mt] = (dim d0, head 2tig), (d0, 2tig+1), (d0+1, 2tig), (d0+1, 2tig+1)
   float m[2], l[2];    // heads 2 tig, 2 tig + 1 (l: this lane's keys until finish_sums)
 
-  // Head grp's dims 32 tig .. (D = 128) as raw bf16 words.
+  // Head grp's dims of lane tig (kdim8 below) as raw bf16 words.
   struct QRaw {
     uint4 v[kLaneDims / 8];
   };
+  // First of the eight dims that lane tig takes for k-steps 2q, 2q + 1.
+  static __device__ __forceinline__ int kdim8(int q, int tig) {
+    return FP8 ? kLaneDims * tig + 8 * q : 32 * q + 8 * tig;
+  }
   // rows[0]: the row of head grp (nullptr: a zero padding head); rows[1] is
   // not used (heads grp + 8 do not exist for g <= 8).
   static __device__ __forceinline__ void fetch_q(const __nv_bfloat16* const (&rows)[2], QRaw& r,
                                                  int tig) {
 #pragma unroll
     for (int i = 0; i < kLaneDims / 8; ++i)
-      r.v[i] = rows[0] ? *reinterpret_cast<const uint4*>(rows[0] + kLaneDims * tig + 8 * i)
+      r.v[i] = rows[0] ? *reinterpret_cast<const uint4*>(rows[0] + kdim8(i, tig))
                        : make_uint4(0u, 0u, 0u, 0u);
   }
   __device__ __forceinline__ void load_q(const __nv_bfloat16* const (&rows)[2], float q_scale,
@@ -507,14 +514,14 @@ struct MmaKeys {
   }
 
   // The K fragments of k-steps 2q, 2q + 1 of key row `row` (lane tig's dims
-  // 8 q .. 8 q + 7 of its run): w[0], w[1] = k-step 2q's (a0|a1, a2|a3 half),
+  // kdim8(q, tig) .. + 7): w[0], w[1] = k-step 2q's (a0|a1, a2|a3 half),
   // w[2], w[3] = k-step 2q + 1's.
   static __device__ __forceinline__ void k_words(const uint8_t* krow, int row, int q, int tig,
                                                  uint32_t (&w)[4]) {
     if constexpr (FP8) {
       // 8 codes: dims kLaneDims tig + 8 q .. + 7, in a 16-byte chunk with the
       // next 8 (swizzled rows at D = 128)
-      const int byte = kLaneDims * tig + 8 * q;
+      const int byte = kdim8(q, tig);
       const int chunk = byte >> 4;
       const uint8_t* src =
           krow + ((kSw ? (chunk ^ (row & 7)) : chunk) << 4) + (byte & 15);
@@ -522,7 +529,7 @@ struct MmaKeys {
       MmaRows<D, FP8>::widen8(x.x, x.y, w);
     } else {
       const uint4 x =
-          *reinterpret_cast<const uint4*>(krow + (kLaneDims * tig + 8 * q) * G::kElt);
+          *reinterpret_cast<const uint4*>(krow + kdim8(q, tig) * G::kElt);
       w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
     }
   }
