@@ -392,7 +392,9 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
     if pa.get_error() != pa.PA_OK:
         raise RuntimeError("device error in the split runs")
     peak_t = load_peaks_tensor()
+    peak_h, peak_kind = load_peaks()
     tf = flops / (ms_pre * 1e-3) / 1e12
+    gbs_dec = dec_bytes / (ms_dec * 1e-3) / 1e9
     del step, sp, sd
     torch.cuda.empty_cache()
     cpu = None
@@ -410,7 +412,11 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
                                       "frac": round(tf / peak_t, 4),
                                       "peak_source": "bf16_tflops (measured, burst)"}},
         "decode_only": {"ms": round(ms_dec, 4), "kv_bytes": int(dec_bytes),
-                        "gbs": round(dec_bytes / (ms_dec * 1e-3) / 1e9, 1)},
+                        "gbs": round(dec_bytes / (ms_dec * 1e-3) / 1e9, 1),
+                        "roofline": {"bound": "hbm", "achieved": round(gbs_dec, 1),
+                                     "peak": peak_h, "unit": "GB/s",
+                                     "frac": round(gbs_dec / peak_h, 4),
+                                     "peak_source": f"hbm_gbs ({peak_kind})"}},
     }
 
 
