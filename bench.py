@@ -411,6 +411,13 @@ def run_mixed(args, dev, cfg, kv_dtype=None):
                                       "peak": peak_t, "unit": "TFLOP/s",
                                       "frac": round(tf / peak_t, 4),
                                       "peak_source": "bf16_tflops (measured, burst)"}},
+        **({"prefill_e4m3_peak": {
+            "peak": round(peak_t * 2 / 2.5, 1), "unit": "TFLOP/s",
+            "frac": round(tf / (peak_t * 2 / 2.5), 4),
+            "how": "the MMA work of an E4M3 pool's chunk: S as three E4M3 products "
+                   "(query split in three terms) at twice the bf16 rate, 1.5 bf16 S "
+                   "equivalents, plus P.V on f16 operands: 2.5 units against bf16's 2, "
+                   "so the measured bf16 peak x 2 / 2.5"}} if w.kv_dtype == "fp8" else {}),
         "decode_only": {"ms": round(ms_dec, 4), "kv_bytes": int(dec_bytes),
                         "gbs": round(dec_bytes / (ms_dec * 1e-3) / 1e9, 1),
                         "roofline": {"bound": "hbm", "achieved": round(gbs_dec, 1),

@@ -119,3 +119,37 @@ def test_error_raised_on_another_stream_is_never_lost(cuda_device):
     assert seen.count(pa.PA_ERR_TIMEOUT) == 1, sorted(set(seen))
     assert all(x in (pa.PA_OK, pa.PA_ERR_TIMEOUT) for x in seen)
     assert pa.get_error() == pa.PA_OK
+
+
+def test_shared_prefix_device_mirror_errors_are_flagged_and_never_written(cuda_device):
+    """pa_forward_shared_prefix with device arrays that disagree with their
+    host mirrors: a group member whose device query_start_loc points past
+    the T rows, and a member whose device seq_len no longer reaches past the
+    shared prefix, raise PA_ERR_DEVICE_BOUNDS; nothing is written beyond row
+    T, and the next call is clean."""
+    from tests.gpu_helpers import group_arrays
+    w = workloads.build([64 + 5, 64 + 30, 64 + 1, 64 + 200, 90], [1] * 5, Hq=8, Hkv=2, D=128,
+                        B=16, seed=8, device=cuda_device, groups=[([0, 1, 2, 3], 64)])
+    step = DeviceStep(w, cuda_device, max_splits=8)
+    step.run(cascade=True)
+    assert pa.get_error() == pa.PA_OK
+    first, size, prefix_blocks = group_arrays(w)
+    big, out = _sentinel_out(step.q, w.T)
+
+    def call(qsl, seq):
+        pa.forward_shared_prefix(step.q, out, qsl, seq, w.qsl, w.seq_lens, step.gathered,
+                                 step.pool, w.scale, first, size, prefix_blocks,
+                                 causal=w.causal, workspace=step.ws)
+
+    bad_qsl = torch.tensor([0, 1, 2, w.T + 2, w.T + 3, w.T], dtype=torch.int32,
+                           device=cuda_device)
+    call(bad_qsl, step.seq)
+    assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS
+    assert (big[w.T:].view(torch.int16) == 0x1234).all()
+    short = step.seq.clone()
+    short[1] = 64  # member 1: no key after the 64-token prefix
+    call(step.qsl, short)
+    assert pa.get_error() == pa.PA_ERR_DEVICE_BOUNDS
+    assert (big[w.T:].view(torch.int16) == 0x1234).all()
+    step.run(cascade=True)
+    assert pa.get_error() == pa.PA_OK
