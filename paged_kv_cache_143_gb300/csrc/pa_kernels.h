@@ -96,6 +96,7 @@ struct DecodeParams {
 };
 
 constexpr int kMaxOrderedPrefill = 256;
+constexpr int kMaxPrefillUnits = 1024;
 
 struct PrefillParams {
   __nv_bfloat16* out;          // [T][Hq][D]
@@ -114,6 +115,12 @@ struct PrefillParams {
   // grid.z walks every request in batch order
   int32_t n_order;
   int32_t order[kMaxOrderedPrefill];
+  // (request, tile pair) units in launch order, the most key tiles first
+  // across all requests: unit = request << 16 | last << 15 | pair, last set
+  // on the request's highest pair. With n_units > 0 the grid is
+  // (Hkv, n_units) and order/n_order are unused.
+  int32_t n_units;
+  int32_t units[kMaxPrefillUnits];
 };
 
 struct PrefillLaunch {

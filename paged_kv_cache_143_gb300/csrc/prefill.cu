@@ -158,30 +158,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + S::kOffBar);
 
-  // a prefill chunk of request r (grid z: the requests, heaviest first)
-  const int r = p.n_order ? p.order[blockIdx.z] : (int)blockIdx.z;
+  // a tile pair of a prefill chunk of request r: from the unit list (grid
+  // (Hkv, units), longest units first; unit = request << 16 | last << 15 |
+  // pair, last marking the request's highest listed pair), else from the
+  // grid (pairs, Hkv, requests), requests heaviest first and each request's
+  // latest pairs first
+  const bool listed = p.n_units > 0;
+  const int unit = listed ? p.units[blockIdx.y] : 0;
+  const int r = listed ? unit >> 16 : p.n_order ? p.order[blockIdx.z] : (int)blockIdx.z;
   const int q_begin = p.qsl[r];
   const int q_len = p.qsl[r + 1] - q_begin;
-  if (q_len <= 1) return;  // decode requests and empty requests are not ours
+  // (one CTA per request reports a bad entry: the first kv head of a unit
+  // on the list, else the request's first grid cell)
+  const bool reporter = threadIdx.x == 0 && blockIdx.x == 0 && (listed || blockIdx.y == 0);
+  if (q_len <= 1) {
+    // decode requests and empty requests are not ours; a listed unit of one
+    // means the device qsl disagrees with the host mirror the list came from
+    if (listed && reporter) raise_error(p.err, kErrBounds);
+    return;
+  }
   const int seq = p.seq_lens[r];
   if (seq < q_len || seq > p.max_blocks * p.B || q_begin < 0 || q_begin + q_len > p.T) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    if (reporter) raise_error(p.err, kErrBounds);
     return;
   }
   const int32_t* table = p.block_tables + (int64_t)r * p.max_blocks;
-  const int pair_x = blockIdx.x;
   const int g = p.g;
   const int tpt = kM / g;  // tokens per tile
   const int ntq = (q_len + tpt - 1) / tpt;
   const int npairs = (ntq + 1) / 2;
-  if (npairs > (int)gridDim.x) {
-    // more query tiles than the grid was planned for: device qsl disagrees
-    // with the host mirror; the tiles past the grid would be left unwritten
-    if (threadIdx.x == 0 && pair_x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+  int pair, kvh;
+  if (listed) {
+    pair = unit & 0x7FFF;
+    kvh = blockIdx.x;
+    // the device qsl disagrees with the host mirror the list was planned
+    // from: a unit past the request's tiles, or tiles past the request's last
+    // listed pair (those would be left unwritten)
+    const bool last_listed = (unit & 0x8000) != 0;
+    if (pair >= npairs || (last_listed && pair != npairs - 1)) {
+      if (reporter) raise_error(p.err, kErrBounds);
+      if (pair >= npairs) return;
+    }
+  } else {
+    const int pair_x = blockIdx.x;
+    if (npairs > (int)gridDim.x) {
+      // more query tiles than the grid was planned for: device qsl disagrees
+      // with the host mirror; the tiles past the grid would be left unwritten
+      if (threadIdx.x == 0 && pair_x == 0 && blockIdx.y == 0) raise_error(p.err, kErrBounds);
+    }
+    if (pair_x >= npairs) return;
+    pair = npairs - 1 - pair_x;  // heaviest (latest) pairs start first
+    kvh = blockIdx.y;
   }
-  if (pair_x >= npairs) return;
-  const int pair = npairs - 1 - pair_x;  // heaviest (latest) pairs start first
-  const int kvh = blockIdx.y;
   const int P = seq - q_len;
   int q0[2], ntk[2], n_kv[2];
 #pragma unroll
@@ -819,8 +847,9 @@ cudaError_t launch_prefill_t(const PrefillLaunch& L, cudaStream_t s) {
   e = cudaFuncGetAttributes(&fa, prefill_kernel<D, F8>);
   if (e != cudaSuccess) return e;
   if (fa.numRegs < (int)kLaunchRegs) return cudaErrorInvalidConfiguration;
-  // tile pairs x kv heads x prefill requests
-  dim3 grid((L.max_q_tiles + 1) / 2, p.Hkv, p.n_order ? p.n_order : L.R);
+  // kv heads x listed units, else tile pairs x kv heads x prefill requests
+  const dim3 grid = p.n_units > 0 ? dim3(p.Hkv, p.n_units, 1)
+                                  : dim3((L.max_q_tiles + 1) / 2, p.Hkv, p.n_order ? p.n_order : L.R);
   prefill_kernel<D, F8><<<grid, kThreads, smem, s>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
