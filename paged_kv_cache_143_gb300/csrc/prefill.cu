@@ -96,7 +96,8 @@ struct Smem {
   static constexpr int kOffK8 = kOffV + kStages * kKVBytes;
   static constexpr int kOffV8 = kOffK8 + kStages * kK8Bytes;
   static constexpr int kOffBar = kOffV8 + kStages * kK8Bytes;
-  static constexpr int kBytes = kOffBar + 256;
+  static constexpr int kBarBytes = 512;               // the mbarriers (struct Bars)
+  static constexpr int kBytes = kOffBar + kBarBytes;
   static constexpr int kAlloc = kBytes + 1024;  // the base is rounded up to 1024 B
   static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB per-block limit");
   static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kKBytes % 1024 == 0,
@@ -157,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + S::kOffBar);
+  static_assert(sizeof(Bars) <= S::kBarBytes, "the mbarriers overrun their shared-memory slot");
 
   // a tile pair of a prefill chunk of request r: from the unit list (grid
   // (Hkv, units), longest units first; unit = request << 16 | last << 15 |
