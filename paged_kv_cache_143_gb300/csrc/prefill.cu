@@ -14,6 +14,9 @@
 // (row = token * g + head), so K/V are read once per group: 128 / g tokens
 // per tile (integer division; when g does not divide 128 the last
 // 128 mod g rows of every tile stay unused, masked to P = 0), g <= 128.
+// The CTAs go out longest first across all requests: the host plans a list
+// of (request, tile pair) units sorted by the key tiles each walks, since the
+// block scheduler hands out CTAs in grid order as SMs free up.
 //   warpgroup 0  warp 0: TMA producer — the Q tiles once (a 4-D tensor map over
 //                [T][Hkv][g][D]), then per 128-key tile one 2-D box per physical
 //                block and 64-column chunk (coordinates from the block table),
