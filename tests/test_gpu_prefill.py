@@ -88,13 +88,16 @@ def test_mixed_chunked_prefill_reduced_full_compare(cuda_device):
     check(w, cuda_device)
 
 
-@pytest.mark.parametrize("n_req,q_len", [(103, 160), (260, 64)], ids=["ordered", "batch-order"])
+@pytest.mark.parametrize("n_req,q_len", [(103, 160), (260, 64), (300, 12)],
+                         ids=["ordered", "batch-order", "listed-many-requests"])
 def test_prefill_launch_orders_past_the_unit_list(cuda_device, n_req, q_len):
-    """More (request, tile pair) units than the launch's unit list holds
-    (1024): g 16 gives 8-token tiles, so 103 chunks of 160 tokens are 1030
-    units (the grid with requests ordered by work) and 260 chunks of 64 are
-    1040 units for more requests than the order holds (the grid in batch
-    order). Prefixes vary so the requests' work differs; every row compared."""
+    """The launch orders around the unit list's capacity (1024 units): g 16
+    gives 8-token tiles, so 103 chunks of 160 tokens are 1030 units (the grid
+    with requests ordered by work), 260 chunks of 64 are 1040 units for more
+    requests than the order holds (the grid in batch order), and 300 chunks
+    of 12 are 300 one-pair units on the list (more requests than the order
+    holds, so listed request ids go past 255). Prefixes vary so the
+    requests' work differs; every row compared."""
     rng = np.random.default_rng(n_req)
     prefix = rng.integers(0, 300, n_req)
     w = workloads.build([int(p) + q_len for p in prefix], [q_len] * n_req, Hq=16, Hkv=1,
