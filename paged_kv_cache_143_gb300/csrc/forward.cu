@@ -12,6 +12,7 @@
 
 #include "pa_internal.h"
 #include "pa_kernels.h"
+#include "prefill_plan.h"
 
 namespace {
 
@@ -338,40 +339,15 @@ pa_status forward_impl(const void* q, void* out, const int32_t* query_start_loc,
   if (n_pre > 0) {
     pa::PrefillLaunch L = prefill_launch();
     L.max_q_tiles = max_q_tiles;
-    // Launch order: a CTA's time grows with the key tiles it walks (those of
-    // the later query tile of its pair), so the (request, tile pair) units
-    // go out longest first across all requests, each unit's kv heads side by
-    // side (the block scheduler hands out CTAs in grid order as SMs free up).
-    // Units past the list's capacity fall back to a (pairs, Hkv, requests)
-    // grid with the requests ordered by their causal pairs.
-    const int tpt = 128 / g;  // tokens per query tile
-    int64_t n_units = 0;
-    for (int r = 0; r < R; ++r) {
-      const int ql = qsl_host[r + 1] - qsl_host[r];
-      if (ql > 1) n_units += ((ql + tpt - 1) / tpt + 1) / 2;
-    }
-    if (n_units <= pa::kMaxPrefillUnits) {
-      struct Unit {
-        int32_t steps, id;
-      };
-      Unit units[pa::kMaxPrefillUnits];
-      int n = 0;
-      for (int r = 0; r < R; ++r) {
-        const int ql = qsl_host[r + 1] - qsl_host[r];
-        if (ql <= 1) continue;
-        const int seq = seq_lens_host[r];
-        const int npairs = ((ql + tpt - 1) / tpt + 1) / 2;
-        for (int pair = npairs - 1; pair >= 0; --pair) {
-          // keys of the pair's later tile: causal, up to its last token
-          const int last = std::min(ql, (2 * pair + 2) * tpt);
-          const int n_kv = causal ? seq - ql + last : seq;
-          const int last_pair = pair == npairs - 1 ? 0x8000 : 0;
-          units[n++] = Unit{(n_kv + 127) / 128, (r << 16) | last_pair | pair};
-        }
-      }
-      std::stable_sort(units, units + n, [](const Unit& a, const Unit& b) { return a.steps > b.steps; });
-      for (int i = 0; i < n; ++i) L.p.units[i] = units[i].id;
-      L.p.n_units = n;
+    // Launch order (prefill_plan.h): the (request, tile pair) units longest
+    // first across all requests, each unit's kv heads side by side. Units
+    // past the list's capacity fall back to a (pairs, Hkv, requests) grid
+    // with the requests ordered by their causal pairs.
+    const int n_units =
+        pa::plan_prefill_units<pa::kMaxPrefillUnits>(qsl_host, seq_lens_host, R, g, causal != 0,
+                                                     L.p.units);
+    if (n_units >= 0) {
+      L.p.n_units = n_units;
     } else if (n_pre <= pa::kMaxOrderedPrefill) {
       int n = 0;
       for (int r = 0; r < R; ++r)
